@@ -1,0 +1,459 @@
+"""Benchmark of the NVFP4 paged KV-cache hot path on GB300.
+
+One step is the whole path over one batch of synthetic input: the global decode scales of
+K and V, quantize-and-append of every token into the paged NVFP4 pool, paged dequantize of
+every request into contiguous bf16, and the FP8 materialize of every active page.
+
+Default workload ("large_pool"): batch 256, lengths U[1024, 16384] (about 2.2 M tokens),
+page_size 16, 8 KV heads, head_dim 128, HND, a ~40 GB pool with the active pages placed at
+random, bf16 N(0, sigma^2) with sigma ~ U[0.5, 4] per (K/V, head), 4over6 MAE with
+e4m3_max 256 and fp16 error. Inputs (9 GB) are larger than L2, so no flush is needed.
+
+Metric: algorithmic HBM bytes of the step (data only; index traffic excluded) / step time,
+in GB/s; per-op GB/s, % of 8 TB/s, % of the measured copy bandwidth and tokens/s as well.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Under torchrun each rank runs its own replica of the workload on its own GPU (the path
+shards by request with no exchange): weak scaling, max time over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "HBM GB/s (% of 8 TB/s) and tokens/s per op: append, dequant_paged, materialize"
+NOMINAL_HBM_GBS = 8000.0
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", 6800.0)), "measured"
+    return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------------------
+# algorithmic bytes (data only) of each op for a workload
+# ---------------------------------------------------------------------------------------
+
+def op_bytes(w: W.Workload, n_active_pages: int):
+    H, D, ps = w.H, w.D, w.ps
+    row = H * D
+    nnz = w.nnz
+    toks = int(np.minimum(w.seq_lens, w.max_seq_len).sum())
+    return {
+        "global_scale": 2 * nnz * row * 2,
+        "append": nnz * H * (4 * D + D + D // 8),
+        "dequant_paged": toks * H * (D + D // 8 + 4 * D),
+        "materialize": n_active_pages * ps * H * (3 * D + D // 8) + 2 * H * ps * D
+        + w.B * (-(-w.max_kv_len // ps)) * 4,
+    }, {"global_scale": nnz, "append": nnz, "dequant_paged": toks,
+        "materialize": n_active_pages * ps}
+
+
+# ---------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, out_path: str):
+        self.path = out_path
+        self.proc = None
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self, t0: float = 0.0, t1: float = float("inf")):
+        """Stop sampling; summarize the samples taken between host times t0 and t1."""
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        want = vis.split(",")[int(os.environ.get("LOCAL_RANK", "0"))] if vis else None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for ln in f:
+                parts = [p.strip() for p in ln.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                except ValueError:
+                    continue
+                if not (t0 - 1.0 <= ts <= t1):
+                    continue
+                parts = parts[1:]
+                if want is not None and want.isdigit() and parts[0] != want:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------
+# the device state of one step
+# ---------------------------------------------------------------------------------------
+
+class Step:
+    """Buffers and launches of one pass of the hot path on the current device."""
+
+    def __init__(self, w: W.Workload, dev: torch.device):
+        import nvfp4_paged_kv_02_gb300 as nv
+        self.nv, self.w, self.dev = nv, w, dev
+        r = w.recipe
+        self.recipe = None if r is None else nv.NVFP44Over6Config(
+            r.e4m3_max, "MSE" if r.err_mode else "MAE", bool(r.err_use_fast_math))
+        t = lambda a: torch.as_tensor(np.ascontiguousarray(a)).to(dev)
+        inner = (w.ps, w.H) if w.layout == W.NHD else (w.H, w.ps)
+        self.cache = tuple(torch.empty((w.num_pages, *inner, w.D // 2), dtype=torch.uint8,
+                                       device=dev) for _ in range(2))
+        self.sf = tuple(torch.empty((w.num_pages, *inner, w.D // 16), dtype=torch.uint8,
+                                    device=dev) for _ in range(2))
+        self.k, self.v = w.k.to(dev), w.v.to(dev)
+        self.bi, self.pos = t(w.batch_indices), t(w.positions)
+        self.kv_indices, self.kv_indptr = t(w.kv_indices), t(w.kv_indptr)
+        self.last = t(w.kv_last_page_len)
+        self.bt, self.seq_lens = t(w.block_tables), t(w.seq_lens)
+        self.mat_bt = t(w.mat_block_tables)
+        self.indptr = None if w.kv_page_indptr is None else t(w.kv_page_indptr)
+        self.out_k = torch.empty((w.B, w.max_seq_len, w.H, w.D), dtype=w.dtype, device=dev)
+        self.out_v = torch.empty_like(self.out_k)
+        n_out, mpps = nv.nvfp4_materialize_fp8_out_pages(w.B, w.max_kv_len, w.ps, w.mat_num_pages)
+        self.fp8 = torch.empty((n_out, 2, w.H, w.ps, w.D), dtype=torch.float8_e4m3fn, device=dev)
+        self.tables = torch.empty((w.B, mpps), dtype=torch.int32, device=dev)
+        self.gk = torch.empty(1, dtype=torch.float32, device=dev)
+        self.gv = torch.empty(1, dtype=torch.float32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.lay = "NHD" if w.layout == W.NHD else "HND"
+        self.launches_per_step = 7  # 2 x (amax + finalize), append, dequant, materialize
+        if w.prefill_k is not None:
+            # rows already in the cache before the measured append (untimed)
+            pk, pv = w.prefill_k.to(dev), w.prefill_v.to(dev)
+            nv.nvfp4_make_global_scale(torch.cat([pk, self.k]), self.recipe, out=self.gk)
+            nv.nvfp4_make_global_scale(torch.cat([pv, self.v]), self.recipe, out=self.gv)
+            nv.nvfp4_quantize_append_paged(
+                pk, pv, t(w.prefill_batch_indices), t(w.prefill_positions), self.cache, self.sf,
+                self.kv_indices, self.kv_indptr, self.last, float(self.gk.item()),
+                float(self.gv.item()), self.lay, self.recipe, self.status)
+            del pk, pv
+
+    def run(self, ev=None):
+        nv, w = self.nv, self.w
+        rec = (lambda i: ev[i].record()) if ev is not None else (lambda i: None)
+        rec(0)
+        nv.nvfp4_make_global_scale(self.k, self.recipe, out=self.gk)
+        nv.nvfp4_make_global_scale(self.v, self.recipe, out=self.gv)
+        rec(1)
+        # the append API takes the scales as host floats
+        gs_k, gs_v = float(self.gk.item()), float(self.gv.item())
+        rec(2)
+        nv.nvfp4_quantize_append_paged(self.k, self.v, self.bi, self.pos, self.cache, self.sf,
+                                       self.kv_indices, self.kv_indptr, self.last, gs_k, gs_v,
+                                       self.lay, self.recipe, self.status)
+        rec(3)
+        nv.nvfp4_dequantize_paged(self.cache, self.sf, self.bt, self.seq_lens, self.gk, self.gv,
+                                  self.out_k, self.out_v, self.lay, self.status)
+        rec(4)
+        nv.nvfp4_materialize_fp8(self.cache[0], self.cache[1], self.sf[0], self.sf[1],
+                                 self.mat_bt, self.seq_lens, w.max_kv_len, w.mat_shared, self.fp8,
+                                 self.indptr, w.mat_num_pages, self.lay, self.tables, True,
+                                 self.status)
+        rec(5)
+
+
+def make_workload(name: str, dev: torch.device) -> W.Workload:
+    if name == "large_pool":
+        return W.large_pool(device=str(dev))
+    return W.NAMED[name]()
+
+
+def active_pages(w: W.Workload) -> int:
+    mpps = -(-w.max_kv_len // w.ps)
+    return int(np.minimum(-(-w.seq_lens.astype(np.int64) // w.ps), mpps).sum())
+
+
+# ---------------------------------------------------------------------------------------
+# the CPU oracle on a bounded sample (baseline and reference arm)
+# ---------------------------------------------------------------------------------------
+
+def oracle_sample(w: W.Workload, n_req: int):
+    """A sub-batch of the workload (its first n_req requests, their rows, a compact pool)
+    as host arrays, plus its algorithmic bytes."""
+    sel = np.arange(min(n_req, w.B))
+    lens = w.seq_lens[sel].astype(np.int64)
+    rows = np.isin(w.batch_indices, sel)
+    sub = W.make_paged("sample", 0, B=len(sel), H=w.H, D=w.D, ps=w.ps, layout=w.layout,
+                       dtype=w.dtype, lens_old=np.zeros(len(sel), np.int64), lens_new=lens,
+                       recipe=w.recipe, sampler=lambda r, n: np.zeros((n, w.H, w.D), np.float32),
+                       max_kv_len=w.max_kv_len, extra_pages=1)
+    sub.k = w.k[torch.from_numpy(np.flatnonzero(rows)).to(w.k.device)].cpu()
+    sub.v = w.v[torch.from_numpy(np.flatnonzero(rows)).to(w.v.device)].cpu()
+    sub.batch_indices = w.batch_indices[rows]
+    sub.positions = w.positions[rows]
+    nb, _ = op_bytes(sub, active_pages(sub))
+    return sub, sum(nb.values())
+
+
+def time_oracle(sub: W.Workload, nthreads: int = 0) -> float:
+    from tests import pipelines as PL
+    t0 = time.perf_counter()
+    PL.run_oracle(sub, nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w: W.Workload, target_s: float = 15.0):
+    import oracle
+    cores = oracle.max_threads()
+    n = 1
+    sub, nbytes = oracle_sample(w, n)
+    dt = time_oracle(sub)
+    while dt < target_s / 4 and n < w.B:
+        n = min(w.B, max(n + 1, int(n * min(8.0, target_s / 2 / max(dt, 1e-3)))))
+        sub, nbytes = oracle_sample(w, n)
+        dt = time_oracle(sub)
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {n} of {w.B} requests ({sub.nnz} tokens) of the {w.name} workload, "
+                      f"whole step, {dt:.1f} s"}
+
+
+def reference_arm(args, w: W.Workload):
+    """The CPU oracle as the reference implementation: K timed steps (after W untimed) on a
+    bounded sample of the same workload."""
+    import oracle
+    n_req = max(1, min(w.B, args.ref_requests))
+    sub, nbytes = oracle_sample(w, n_req)
+    for _ in range(args.warmup):
+        time_oracle(sub)
+    times = [time_oracle(sub) for _ in range(args.steps)]
+    dt = sum(times) / len(times)
+    v = nbytes / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": w.name, "sample_requests": n_req,
+                                            "sample_tokens": sub.nnz},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": oracle.max_threads(),
+                             "kind": "oracle",
+                             "sample": f"first {n_req} of {w.B} requests ({sub.nnz} tokens), "
+                                       f"whole step per timed step"},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="large_pool",
+                    choices=["large_pool", "decode", "prefill", "materialize", "tiny"])
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--ref-requests", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if args.impl == "reference":
+        if rank == 0:
+            w = make_workload(args.workload, torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu"))
+            reference_arm(args, w)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import nvfp4_paged_kv_02_gb300 as nv
+    nv.load()
+    w = make_workload(args.workload, dev)
+    step = Step(w, dev)
+    nbytes, ntok = op_bytes(w, active_pages(w))
+    total_bytes = sum(nbytes.values())
+    small = total_bytes < 4 * 129e6
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if small else None
+
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize(dev)
+    if int(step.status.item()) != 0:
+        raise SystemExit(f"device status {int(step.status.item()):#x} after warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    clocks.start()
+    time.sleep(0.5)  # let the sampler come up before the timed region
+    torch.cuda.synchronize(dev)
+    step_ms = []
+    h0 = time.time()
+    for s in range(args.steps):
+        if flush is not None:
+            flush.fill_(s & 0xFF)
+        step.run(evs[s])
+    torch.cuda.synchronize(dev)
+    h1 = time.time()
+    clk = clocks.stop(h0, h1)
+    for s in range(args.steps):
+        step_ms.append(evs[s][0].elapsed_time(evs[s][5]))
+    ms = float(np.mean(step_ms))
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+        dist.barrier()
+    # per-op device time (mean over steps)
+    seg = {"global_scale": (0, 1), "append": (2, 3), "dequant_paged": (3, 4), "materialize": (4, 5)}
+    op_ms = {k: float(np.mean([evs[s][a].elapsed_time(evs[s][b]) for s in range(args.steps)]))
+             for k, (a, b) in seg.items()}
+    peak, peak_kind = measured_peaks()
+    ops = {}
+    for k in seg:
+        gbs = nbytes[k] / (op_ms[k] * 1e-3) / 1e9
+        ops[k] = {"us": op_ms[k] * 1e3, "bytes": nbytes[k], "GB_s": gbs,
+                  "pct_of_8TBs": 100 * gbs / NOMINAL_HBM_GBS,
+                  "pct_of_measured_copy": 100 * gbs / peak,
+                  "tokens_per_s": ntok[k] / (op_ms[k] * 1e-3)}
+    dom = max(("append", "dequant_paged", "materialize"), key=lambda k: op_ms[k])
+    value = world * total_bytes / (ms * 1e-3) / 1e9
+    status = int(step.status.item())
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(step, w, args, total_bytes, world)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.B, "tokens": w.nnz, "page_size": w.ps,
+                       "num_kv_heads": w.H, "head_dim": w.D,
+                       "kv_layout": "NHD" if w.layout == W.NHD else "HND",
+                       "input_dtype": str(w.dtype).replace("torch.", ""),
+                       "recipe": None if w.recipe is None else vars(w.recipe),
+                       "pool_pages": w.num_pages, "active_pages": active_pages(w),
+                       "l2": "flushed with a 256 MB write between steps" if small
+                       else "inputs larger than L2 (129 MB); no flush",
+                       "parallelism": f"replicas x{world}"},
+            "ops": ops,
+            "roofline": {"bound": "hbm", "kernel": dom,
+                         "achieved": nbytes[dom] / (op_ms[dom] * 1e-3) / 1e9,
+                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": nbytes[dom] / (op_ms[dom] * 1e-3) / 1e9 / peak,
+                         "traffic": None},
+            "clocks": clk, "gpu_launches": step.launches_per_step * args.steps,
+            "e2e": e2e, "cpu_baseline": cpu, "device_status": status,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def measure_e2e(step: Step, w: W.Workload, args, total_bytes: int, world: int):
+    """The same step through the public API with the appended K/V rows in pinned host
+    memory: each step copies them to the device, runs the path and reads back the step's
+    summary (the two global scales and the device status word)."""
+    dev = step.dev
+    hk = torch.empty(step.k.shape, dtype=step.k.dtype, pin_memory=True)
+    hv = torch.empty(step.v.shape, dtype=step.v.dtype, pin_memory=True)
+    hk.copy_(step.k)
+    hv.copy_(step.v)
+    res = torch.empty(3, dtype=torch.float32, pin_memory=True)
+    summary = torch.empty(3, dtype=torch.float32, device=dev)
+
+    def one():
+        step.k.copy_(hk, non_blocking=True)
+        step.v.copy_(hv, non_blocking=True)
+        step.run()
+        summary[0] = step.gk[0]
+        summary[1] = step.gv[0]
+        summary[2] = step.status[0].float()
+        res.copy_(summary, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    n = max(2, min(args.steps, 5))
+    a.record()
+    for _ in range(n):
+        one()
+    b.record()
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / n
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    h2d = hk.numel() * hk.element_size() + hv.numel() * hv.element_size()
+    return {"value": world * total_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 12, "ms_per_step": ms}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,368 @@
+"""GB300 (sm_103a) NVFP4 paged KV-cache operations.
+
+A thin ctypes binding over ``libnvfp4kv.so`` (C ABI in ``include/nvfp4kv.h``): it only
+turns torch tensors into pointers, strides and the current CUDA stream. Every step of the
+work runs in the library's CUDA kernels; there is no fallback of any kind, and using an op
+without the built library raises.
+
+Operations (FlashInfer documentation pages):
+  nvfp4_quantize_append_paged  "flashinfer.page.nvfp4_quantize_append_paged_kv_cache"
+  nvfp4_dequantize_paged       "flashinfer.quantization.nvfp4_kv_dequantize_paged"
+  nvfp4_materialize_fp8        "...kernels.nvfp4_kv_materialize.nvfp4_kv_materialize_fp8"
+  NVFP4KVMaterializer          "flashinfer.quantization" index, NVFP4KVMaterializer
+  nvfp4_make_global_scale      "flashinfer.quantization" index, make_nvfp4_global_scale
+  nvfp4_e4m3_max               "flashinfer.quantization" index, nvfp4_e4m3_max
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+from typing import Optional, Sequence, Tuple, Union
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "NVFP44Over6Config", "NVFP4KVError", "PagedCache", "load", "nvfp4_e4m3_max",
+    "nvfp4_make_global_scale", "nvfp4_quantize_append_paged", "nvfp4_dequantize_paged",
+    "nvfp4_materialize_fp8", "nvfp4_materialize_fp8_out_pages", "NVFP4KVMaterializer",
+    "paged_caches", "LIB_PATH",
+]
+
+LIB_PATH = _build.LIB_PATH
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_CUDA = 0, 1, 2, 3, 4
+F16, BF16 = 0, 1
+NHD, HND = 0, 1
+I32, I64 = 0, 1
+DEV_BAD_BATCH, DEV_BAD_POSITION, DEV_BAD_PAGE, DEV_LEN_CLAMPED, DEV_BAD_OUT_PAGE = 1, 2, 4, 8, 16
+
+
+class NVFP4KVError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} failed with status {code}: {msg}")
+        self.code = code
+
+
+class _Cache(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("sf", ctypes.c_void_p),
+                ("data_page_stride", ctypes.c_int64), ("sf_page_stride", ctypes.c_int64),
+                ("num_pages", ctypes.c_int64)]
+
+
+class _Config(ctypes.Structure):
+    _fields_ = [("e4m3_max", ctypes.c_float), ("err_mode", ctypes.c_int32),
+                ("err_use_fast_math", ctypes.c_int32)]
+
+
+@dataclass(frozen=True)
+class NVFP44Over6Config:
+    """A 4over6 recipe. Defaults: the full E4M3 range and summed absolute error, evaluated
+    in fp32 (the pages name e4m3_max=256 and err_mode="MSE" as the knobs to turn)."""
+    e4m3_max: float = 448.0
+    err_mode: str = "MAE"
+    err_use_fast_math: bool = False
+
+    def _c(self) -> _Config:
+        mode = {"MAE": 0, "MSE": 1}[self.err_mode.upper()]
+        return _Config(float(self.e4m3_max), mode, int(bool(self.err_use_fast_math)))
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Build (if stale) and load libnvfp4kv.so. Raises if it cannot be built or loaded."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+        L.nvfp4_abi_version.restype = i32
+        L.nvfp4_last_error_string.restype = ctypes.c_char_p
+        L.nvfp4_e4m3_max.restype = f32
+        L.nvfp4_e4m3_max.argtypes = [vp]
+        L.nvfp4_make_global_scale.restype = i32
+        L.nvfp4_make_global_scale.argtypes = [vp, i32, i64, vp, vp, vp]
+        L.nvfp4_quantize_append_paged.restype = i32
+        L.nvfp4_quantize_append_paged.argtypes = [
+            vp, vp, i32, i64, i32, i32, i64, i64, vp, vp, _Cache, _Cache, i32, i32, vp, i64, vp,
+            vp, i32, f32, f32, vp, vp, vp]
+        L.nvfp4_dequantize_paged.restype = i32
+        L.nvfp4_dequantize_paged.argtypes = [
+            _Cache, _Cache, i32, i32, i32, i32, vp, i32, i32, vp, i32, vp, vp, vp, vp, i32, i32,
+            vp, vp]
+        L.nvfp4_materialize_fp8_out_pages.restype = i32
+        L.nvfp4_materialize_fp8_out_pages.argtypes = [i32, i32, i32, i64, vp, vp]
+        L.nvfp4_materialize_fp8.restype = i32
+        L.nvfp4_materialize_fp8.argtypes = [
+            _Cache, _Cache, i32, i32, i32, i32, vp, i32, i32, vp, i32, i32, vp, i64, vp, i64, vp,
+            i32, vp, vp]
+        _lib = L
+        return L
+
+
+def _check(fn: str, code: int) -> None:
+    if code != OK:
+        msg = load().nvfp4_last_error_string().decode(errors="replace")
+        raise NVFP4KVError(fn, code, msg)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("nvfp4 ops take CUDA tensors only")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _layout(kv_layout: Union[str, int]) -> int:
+    if isinstance(kv_layout, int):
+        return kv_layout
+    return {"NHD": NHD, "HND": HND}[kv_layout.upper()]
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float16:
+        return F16
+    if dt == torch.bfloat16:
+        return BF16
+    raise ValueError(f"expected float16 or bfloat16, got {dt}")
+
+
+def _recipe(r: Optional[NVFP44Over6Config]):
+    return None if r is None else ctypes.pointer(r._c())
+
+
+@dataclass
+class PagedCache:
+    """One paged NVFP4 cache (K or V): codes and scales with their page strides (bytes)."""
+    data: torch.Tensor
+    sf: torch.Tensor
+    data_page_stride: int
+    sf_page_stride: int
+    num_pages: int
+
+    def _c(self) -> _Cache:
+        return _Cache(self.data.data_ptr(), self.sf.data_ptr(), self.data_page_stride,
+                      self.sf_page_stride, self.num_pages)
+
+
+def _one_cache(data: torch.Tensor, sf: torch.Tensor) -> PagedCache:
+    if data.dtype != torch.uint8 or sf.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise ValueError("paged caches are uint8 codes and uint8 / float8_e4m3fn scales")
+    if data.dim() != 4 or sf.dim() != 4:
+        raise ValueError("a paged cache tensor is 4-D [pages, ., ., head_dim // 2|16]")
+    for t in (data, sf):
+        if t.stride(3) != 1 or t.stride(2) != t.shape[3] or t.stride(1) != t.shape[2] * t.shape[3]:
+            raise ValueError("paged cache pages must be contiguous inside (page stride may be larger)")
+    return PagedCache(data, sf, data.stride(0) * data.element_size(), sf.stride(0) * sf.element_size(),
+                      data.shape[0])
+
+
+def paged_caches(paged_kv_cache, kv_cache_sf) -> Tuple[PagedCache, PagedCache]:
+    """(K, V) caches from the pages' tuple form (two 4-D tensors each) or stacked 5-D form
+    (K/V on the second dimension)."""
+    if isinstance(paged_kv_cache, (tuple, list)):
+        return (_one_cache(paged_kv_cache[0], kv_cache_sf[0]),
+                _one_cache(paged_kv_cache[1], kv_cache_sf[1]))
+    d, s = paged_kv_cache, kv_cache_sf
+    if d.dim() != 5 or s.dim() != 5 or d.shape[1] != 2 or s.shape[1] != 2:
+        raise ValueError("a stacked cache is 5-D with K/V on the second dimension")
+    # the views' data pointers already carry V's offset inside each page
+    return _one_cache(d[:, 0], s[:, 0]), _one_cache(d[:, 1], s[:, 1])
+
+
+def _dims(cache: PagedCache, layout: int):
+    t = cache.data
+    if layout == NHD:
+        return t.shape[1], t.shape[2], t.shape[3] * 2   # page_size, H, D
+    return t.shape[2], t.shape[1], t.shape[3] * 2
+
+
+def nvfp4_e4m3_max(nvfp4_4over6_config: Optional[NVFP44Over6Config] = None) -> float:
+    """Block-scale clamp implied by a resolved recipe: 448 standard, e4m3_max under 4over6."""
+    return float(load().nvfp4_e4m3_max(_recipe(nvfp4_4over6_config)))
+
+
+def nvfp4_make_global_scale(x: torch.Tensor,
+                            nvfp4_4over6_config: Optional[NVFP44Over6Config] = None,
+                            out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Per-tensor global decode scale amax(|x|) / (6 * e4m3_max), as a 1-element fp32
+    CUDA tensor (1.0 for an all-zero tensor)."""
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    if out is None:
+        out = torch.empty(1, dtype=torch.float32, device=x.device)
+    _check("nvfp4_make_global_scale", load().nvfp4_make_global_scale(
+        _ptr(x), _dtype_code(x.dtype), x.numel(), _recipe(nvfp4_4over6_config), _ptr(out),
+        _stream(x.device)))
+    return out
+
+
+def nvfp4_quantize_append_paged(append_key: torch.Tensor, append_value: torch.Tensor,
+                                batch_indices: torch.Tensor, positions: torch.Tensor,
+                                paged_kv_cache, kv_cache_sf, kv_indices: torch.Tensor,
+                                kv_indptr: torch.Tensor, kv_last_page_len: Optional[torch.Tensor],
+                                k_scale: float, v_scale: float, kv_layout: str = "NHD",
+                                nvfp4_4over6: Optional[NVFP44Over6Config] = None,
+                                dev_status: Optional[torch.Tensor] = None) -> None:
+    """Quantize [nnz, H, D] fp16/bf16 K/V rows and write them into the paged caches."""
+    layout = _layout(kv_layout)
+    kc, vc = paged_caches(paged_kv_cache, kv_cache_sf)
+    ps, H, D = _dims(kc, layout)
+    if append_key.dim() != 3 or append_key.shape != append_value.shape:
+        raise ValueError("append_key/append_value must both be [nnz, num_kv_heads, head_dim]")
+    if append_key.dtype != append_value.dtype:
+        raise ValueError("append_key and append_value must have the same dtype")
+    nnz = append_key.shape[0]
+    for t in (append_key, append_value):
+        if t.shape[1:] != (H, D) or t.stride(2) != 1 or t.stride(1) != D:
+            raise ValueError("append rows must be [nnz, H, D] with heads and elements contiguous")
+    for t in (batch_indices, positions, kv_indices, kv_indptr):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError("index tensors must be contiguous int32")
+    if kv_last_page_len is not None and kv_last_page_len.dtype != torch.int32:
+        raise ValueError("kv_last_page_len must be int32")
+    B = kv_indptr.numel() - 1
+    _check("nvfp4_quantize_append_paged", load().nvfp4_quantize_append_paged(
+        _ptr(append_key), _ptr(append_value), _dtype_code(append_key.dtype), nnz, H, D,
+        append_key.stride(0) if nnz else H * D, append_value.stride(0) if nnz else H * D,
+        _ptr(batch_indices), _ptr(positions), kc._c(), vc._c(), ps, layout, _ptr(kv_indices),
+        kv_indices.numel(), _ptr(kv_indptr), _ptr(kv_last_page_len), B, float(k_scale),
+        float(v_scale),
+        _recipe(nvfp4_4over6), _ptr(dev_status), _stream(append_key.device)))
+
+
+def nvfp4_dequantize_paged(paged_kv_cache, kv_cache_sf, block_tables: torch.Tensor,
+                           seq_lens: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
+                           output_k: torch.Tensor, output_v: torch.Tensor,
+                           kv_layout: str = "NHD",
+                           dev_status: Optional[torch.Tensor] = None) -> None:
+    """Gather and dequantize pages into contiguous [B, max_seq_len, H, D] outputs; positions
+    >= seq_lens are left unchanged."""
+    layout = _layout(kv_layout)
+    kc, vc = paged_caches(paged_kv_cache, kv_cache_sf)
+    ps, H, D = _dims(kc, layout)
+    if block_tables.dim() != 2 or block_tables.dtype not in (torch.int32, torch.int64) \
+            or not block_tables.is_contiguous():
+        raise ValueError("block_tables must be a contiguous [batch, max_pages] int32/int64 tensor")
+    if seq_lens.dtype != torch.int32 or not seq_lens.is_contiguous():
+        raise ValueError("seq_lens must be contiguous int32")
+    for o in (output_k, output_v):
+        if o.dim() != 4 or not o.is_contiguous() or o.shape[2:] != (H, D):
+            raise ValueError("outputs must be contiguous [batch, max_seq_len, H, D]")
+    if output_k.shape != output_v.shape or output_k.dtype != output_v.dtype:
+        raise ValueError("output_k and output_v must match")
+    for s in (k_scale, v_scale):
+        if s.dtype != torch.float32 or s.numel() < 1:
+            raise ValueError("k_scale/v_scale must be float32 CUDA tensors")
+    B, L = output_k.shape[0], output_k.shape[1]
+    _check("nvfp4_dequantize_paged", load().nvfp4_dequantize_paged(
+        kc._c(), vc._c(), ps, H, D, layout, _ptr(block_tables),
+        I64 if block_tables.dtype == torch.int64 else I32, block_tables.shape[1],
+        _ptr(seq_lens), B, _ptr(k_scale), _ptr(v_scale), _ptr(output_k), _ptr(output_v),
+        _dtype_code(output_k.dtype), L, _ptr(dev_status), _stream(output_k.device)))
+
+
+def nvfp4_materialize_fp8_out_pages(batch_size: int, max_kv_len: int, page_size: int,
+                                    num_pages: Optional[int] = None) -> Tuple[int, int]:
+    """(pages of the FP8 copy, max_pages_per_seq)."""
+    n = ctypes.c_int64()
+    m = ctypes.c_int32()
+    _check("nvfp4_materialize_fp8_out_pages", load().nvfp4_materialize_fp8_out_pages(
+        batch_size, max_kv_len, page_size, -1 if num_pages is None else num_pages,
+        ctypes.byref(n), ctypes.byref(m)))
+    return n.value, m.value
+
+
+def nvfp4_materialize_fp8(k_cache: torch.Tensor, v_cache: torch.Tensor,
+                          k_block_scales: torch.Tensor, v_block_scales: torch.Tensor,
+                          block_tables: torch.Tensor, seq_lens: torch.Tensor, max_kv_len: int,
+                          uses_shared_paged_kv_idx: bool = True,
+                          out: Optional[torch.Tensor] = None,
+                          kv_page_indptr: Optional[torch.Tensor] = None,
+                          num_pages: Optional[int] = None, kv_layout: str = "HND",
+                          fp8_block_tables: Optional[torch.Tensor] = None,
+                          zero_fp8_block_tables: bool = True,
+                          dev_status: Optional[torch.Tensor] = None):
+    """Materialize the active pages as FP8 E4M3. Returns (kv_cache_fp8, fp8_block_tables)
+    with kv_cache_fp8 [num_pages + 1, 2, H, page_size, D] (page 0 zero) and
+    fp8_block_tables [batch, max_pages_per_seq] int32 (padding 0)."""
+    layout = _layout(kv_layout)
+    kc = _one_cache(k_cache, k_block_scales)
+    vc = _one_cache(v_cache, v_block_scales)
+    ps, H, D = _dims(kc, layout)
+    B = seq_lens.numel()
+    if kv_page_indptr is not None and num_pages is None:
+        raise ValueError("kv_page_indptr requires num_pages")
+    n_out, mpps = nvfp4_materialize_fp8_out_pages(B, max_kv_len, ps, num_pages)
+    dev = k_cache.device
+    if out is None:
+        out = torch.empty((n_out, 2, H, ps, D), dtype=torch.float8_e4m3fn, device=dev)
+    if out.dim() != 5 or out.shape[1:] != (2, H, ps, D) or not out.is_contiguous():
+        raise ValueError("out must be contiguous [num_out_pages, 2, H, page_size, head_dim]")
+    if fp8_block_tables is None:
+        fp8_block_tables = torch.zeros((B, mpps), dtype=torch.int32, device=dev)
+    if fp8_block_tables.shape != (B, mpps) or fp8_block_tables.dtype != torch.int32 \
+            or not fp8_block_tables.is_contiguous():
+        raise ValueError("fp8_block_tables must be contiguous int32 [batch, max_pages_per_seq]")
+    if block_tables.dtype != torch.int32 or not block_tables.is_contiguous():
+        raise ValueError("block_tables must be contiguous int32")
+    shared = bool(uses_shared_paged_kv_idx)
+    if block_tables.dim() != (2 if shared else 3) or (not shared and block_tables.shape[1] != 2):
+        raise ValueError("block_tables is [batch, max_num_pages] (shared) or [batch, 2, max_num_pages]")
+    _check("nvfp4_materialize_fp8", load().nvfp4_materialize_fp8(
+        kc._c(), vc._c(), ps, H, D, layout, _ptr(block_tables), block_tables.shape[-1],
+        int(shared), _ptr(seq_lens), B, int(max_kv_len), _ptr(kv_page_indptr),
+        -1 if num_pages is None else int(num_pages), _ptr(out), out.shape[0],
+        _ptr(fp8_block_tables), int(bool(zero_fp8_block_tables)), _ptr(dev_status),
+        _stream(dev)))
+    return out, fp8_block_tables
+
+
+class NVFP4KVMaterializer:
+    """Validate once, launch many times ("NVFP4KVMaterializer"): the static layout and the
+    device are checked at construction; run() launches on the current stream with
+    caller-owned outputs, allocates nothing and does not synchronize, so it can be captured
+    in a CUDA graph. It writes only the active table entries (the caller zeroes the table
+    once per step)."""
+
+    def __init__(self, num_kv_heads: int, page_size: int, head_dim: int,
+                 device: Union[str, int, torch.device] = "cuda",
+                 uses_shared_paged_kv_idx: bool = True, kv_layout: str = "HND"):
+        if page_size % 4 != 0:
+            raise ValueError("page_size must be divisible by 4")
+        if head_dim % 64 != 0:
+            raise ValueError("head_dim must be divisible by 64")
+        self.H, self.ps, self.D = num_kv_heads, page_size, head_dim
+        self.device = torch.device(device)
+        if self.device.type != "cuda":
+            raise ValueError("NVFP4KVMaterializer needs a CUDA device")
+        self.shared = bool(uses_shared_paged_kv_idx)
+        self.layout = _layout(kv_layout)
+        self._lib = load()
+
+    def run(self, k_cache, v_cache, k_block_scales, v_block_scales, block_tables, seq_lens,
+            kv_page_indptr, *, out: torch.Tensor, fp8_block_tables: torch.Tensor,
+            dev_status: Optional[torch.Tensor] = None):
+        B, mpps = fp8_block_tables.shape
+        kc = _one_cache(k_cache, k_block_scales)
+        vc = _one_cache(v_cache, v_block_scales)
+        _check("nvfp4_materialize_fp8", self._lib.nvfp4_materialize_fp8(
+            kc._c(), vc._c(), self.ps, self.H, self.D, self.layout, _ptr(block_tables),
+            block_tables.shape[-1], int(self.shared), _ptr(seq_lens), B, mpps * self.ps,
+            _ptr(kv_page_indptr), out.shape[0] - 1, _ptr(out), out.shape[0],
+            _ptr(fp8_block_tables), 0, _ptr(dev_status), _stream(self.device)))
+        return out, fp8_block_tables

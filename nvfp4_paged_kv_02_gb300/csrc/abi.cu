@@ -1,0 +1,352 @@
+// abi.cu -- the extern "C" entry points of libnvfp4kv: host-side validation (the checks the
+// FlashInfer materializer's launcher makes -- dtypes, ranks, inner strides, 16-byte
+// alignment and shared extents -- plus the scale values passed by value), then one
+// launch sequence on the caller's stream.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <sstream>
+#include <unordered_map>
+
+#include "internal.h"
+
+namespace nvfp4 {
+
+namespace {
+thread_local std::string t_error;
+}
+
+void set_error(const std::string& msg) { t_error = msg; }
+void clear_error() { t_error.clear(); }
+nvfp4_status fail(nvfp4_status code, const std::string& msg) {
+  t_error = msg;
+  return code;
+}
+
+nvfp4_status check_launch(const char* what) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+  return NVFP4_OK;
+}
+
+namespace {
+std::mutex g_mu;
+std::unordered_map<int, int> g_sms;
+std::unordered_map<std::string, int> g_occ;
+
+int current_device() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return dev;
+}
+}  // namespace
+
+int sm_count() {
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_sms.find(dev);
+  if (it != g_sms.end()) return it->second;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+  g_sms[dev] = n;
+  return n;
+}
+
+int blocks_per_sm(const void* kernel, int threads, size_t smem) {
+  const int dev = current_device();
+  std::ostringstream key;
+  key << dev << ':' << kernel << ':' << threads << ':' << smem;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_occ.find(key.str());
+    if (it != g_occ.end()) return it->second;
+  }
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = 1;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_occ[key.str()] = n;
+  return n;
+}
+
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+nvfp4_status check_recipe(const nvfp4_4over6_config* r) {
+  if (!r) return NVFP4_OK;
+  if (!(std::isfinite(r->e4m3_max) && r->e4m3_max > 0.0f && r->e4m3_max <= 448.0f))
+    return fail(NVFP4_ERR_INVALID_ARG, "recipe.e4m3_max must be in (0, 448]");
+  if (r->err_mode != NVFP4_ERR_MAE && r->err_mode != NVFP4_ERR_MSE)
+    return fail(NVFP4_ERR_INVALID_ARG, "recipe.err_mode must be NVFP4_ERR_MAE or NVFP4_ERR_MSE");
+  if (r->err_use_fast_math != 0 && r->err_use_fast_math != 1)
+    return fail(NVFP4_ERR_INVALID_ARG, "recipe.err_use_fast_math must be 0 or 1");
+  return NVFP4_OK;
+}
+
+nvfp4_status check_geometry(const char* fn, int32_t page_size, int32_t H, int32_t D,
+                            int32_t layout) {
+  std::string f(fn);
+  if (page_size < 1) return fail(NVFP4_ERR_INVALID_ARG, f + ": page_size must be >= 1");
+  if (H < 1) return fail(NVFP4_ERR_INVALID_ARG, f + ": num_kv_heads must be >= 1");
+  if (D < 16 || D % 16 != 0) return fail(NVFP4_ERR_INVALID_ARG, f + ": head_dim must be a positive multiple of 16");
+  if (layout != NVFP4_NHD && layout != NVFP4_HND)
+    return fail(NVFP4_ERR_INVALID_ARG, f + ": kv_layout must be NVFP4_NHD or NVFP4_HND");
+  const int64_t page_elems = static_cast<int64_t>(page_size) * H * D;
+  if (page_elems > (int64_t(1) << 30))
+    return fail(NVFP4_ERR_UNSUPPORTED, f + ": page_size * num_kv_heads * head_dim above 2^30");
+  return NVFP4_OK;
+}
+
+nvfp4_status check_cache(const char* fn, const char* name, const nvfp4_paged_cache& c,
+                         int32_t page_size, int32_t H, int32_t D) {
+  std::string f = std::string(fn) + ": " + name;
+  const int64_t data_bytes = static_cast<int64_t>(page_size) * H * (D / 2);
+  const int64_t sf_bytes = static_cast<int64_t>(page_size) * H * (D / 16);
+  if (c.num_pages < 0) return fail(NVFP4_ERR_INVALID_ARG, f + ".num_pages must be >= 0");
+  if (c.num_pages > 0 && (!c.data || !c.sf)) return fail(NVFP4_ERR_INVALID_ARG, f + ": null data or sf pointer");
+  if (c.data_page_stride < data_bytes)
+    return fail(NVFP4_ERR_INVALID_ARG, f + ".data_page_stride is smaller than a page");
+  if (c.sf_page_stride < sf_bytes)
+    return fail(NVFP4_ERR_INVALID_ARG, f + ".sf_page_stride is smaller than a page");
+  if (!aligned(c.data, 16) || c.data_page_stride % 16 != 0)
+    return fail(NVFP4_ERR_ALIGNMENT, f + ": data must be 16-byte aligned with a page stride that is a multiple of 16");
+  return NVFP4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+NVFP4_EXPORT int32_t nvfp4_abi_version(void) { return NVFP4KV_ABI_VERSION; }
+
+NVFP4_EXPORT const char* nvfp4_last_error_string(void) { return t_error.c_str(); }
+
+NVFP4_EXPORT float nvfp4_e4m3_max(const nvfp4_4over6_config* recipe) {
+  return recipe ? recipe->e4m3_max : 448.0f;
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_make_global_scale(const void* x, int32_t dtype, int64_t numel,
+                                                  const nvfp4_4over6_config* recipe,
+                                                  float* scale_out, void* stream) {
+  clear_error();
+  if (nvfp4_status st = check_recipe(recipe)) return st;
+  if (dtype != NVFP4_F16 && dtype != NVFP4_BF16)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_make_global_scale: dtype must be NVFP4_F16 or NVFP4_BF16");
+  if (numel < 0) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_make_global_scale: numel must be >= 0");
+  if (!scale_out) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_make_global_scale: scale_out is null");
+  if (numel > 0 && !x) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_make_global_scale: x is null");
+  if (!aligned(x, 16) || !aligned(scale_out, 4))
+    return fail(NVFP4_ERR_ALIGNMENT, "nvfp4_make_global_scale: x must be 16-byte aligned");
+  const float denom = 6.0f * nvfp4_e4m3_max(recipe);
+  return launch_global_scale(x, dtype == NVFP4_BF16, numel, denom, scale_out,
+                             static_cast<cudaStream_t>(stream));
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_quantize_append_paged(
+    const void* append_key, const void* append_value, int32_t dtype, int64_t nnz,
+    int32_t num_kv_heads, int32_t head_dim, int64_t key_row_stride, int64_t value_row_stride,
+    const int32_t* batch_indices, const int32_t* positions, nvfp4_paged_cache k_cache,
+    nvfp4_paged_cache v_cache, int32_t page_size, int32_t kv_layout,
+    const int32_t* kv_indices, int64_t num_kv_indices, const int32_t* kv_indptr,
+    const int32_t* kv_last_page_len, int32_t batch_size, float k_scale, float v_scale,
+    const nvfp4_4over6_config* recipe, int32_t* dev_status, void* stream) {
+  clear_error();
+  const char* fn = "nvfp4_quantize_append_paged";
+  if (nvfp4_status st = check_recipe(recipe)) return st;
+  if (nvfp4_status st = check_geometry(fn, page_size, num_kv_heads, head_dim, kv_layout)) return st;
+  if (dtype != NVFP4_F16 && dtype != NVFP4_BF16)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_quantize_append_paged: dtype must be NVFP4_F16 or NVFP4_BF16");
+  if (nnz < 0) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_quantize_append_paged: nnz must be >= 0");
+  if (batch_size < 0) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_quantize_append_paged: batch_size must be >= 0");
+  if (!(std::isfinite(k_scale) && k_scale > 0.0f) || !(std::isfinite(v_scale) && v_scale > 0.0f))
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_quantize_append_paged: k_scale and v_scale must be positive finite");
+  if (nvfp4_status st = check_cache(fn, "k_cache", k_cache, page_size, num_kv_heads, head_dim)) return st;
+  if (nvfp4_status st = check_cache(fn, "v_cache", v_cache, page_size, num_kv_heads, head_dim)) return st;
+  if (nnz == 0) return NVFP4_OK;
+  const int64_t row_elems = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (key_row_stride < row_elems || value_row_stride < row_elems)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_quantize_append_paged: row strides must cover num_kv_heads * head_dim elements");
+  if (!append_key || !append_value || !batch_indices || !positions || !kv_indptr ||
+      (!kv_indices && num_kv_indices > 0))
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_quantize_append_paged: null device pointer");
+  if (!aligned(append_key, 16) || !aligned(append_value, 16) || key_row_stride % 8 != 0 ||
+      value_row_stride % 8 != 0)
+    return fail(NVFP4_ERR_ALIGNMENT, "nvfp4_quantize_append_paged: inputs must be 16-byte aligned with row strides a multiple of 8 elements");
+  if (batch_size == 0) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_quantize_append_paged: rows given but batch_size is 0");
+  if (num_kv_indices < 0) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_quantize_append_paged: num_kv_indices must be >= 0");
+
+  AppendArgs a{};
+  a.k = static_cast<const uint8_t*>(append_key);
+  a.v = static_cast<const uint8_t*>(append_value);
+  a.k_row_bytes = key_row_stride * 2;
+  a.v_row_bytes = value_row_stride * 2;
+  a.nnz = nnz;
+  a.H = num_kv_heads;
+  a.D = head_dim;
+  a.nb = head_dim / 16;
+  a.div_nb = make_div(a.nb);
+  a.div_H = make_div(num_kv_heads);
+  a.div_ps = make_div(page_size);
+  a.batch_indices = batch_indices;
+  a.positions = positions;
+  a.kc = k_cache;
+  a.vc = v_cache;
+  a.ps = page_size;
+  a.layout = kv_layout;
+  a.kv_indices = kv_indices;
+  a.num_kv_indices = num_kv_indices;
+  a.kv_indptr = kv_indptr;
+  a.kv_last_page_len = kv_last_page_len;
+  a.batch_size = batch_size;
+  a.gs[0] = k_scale;
+  a.gs[1] = v_scale;
+  a.cap_a = nvfp4_e4m3_max(recipe);
+  a.status = dev_status;
+  int mode = 0;
+  if (recipe) mode = 1 + (recipe->err_mode == NVFP4_ERR_MSE ? 1 : 0) + (recipe->err_use_fast_math ? 2 : 0);
+  const bool vec256 = aligned(append_key, 32) && aligned(append_value, 32) &&
+                      key_row_stride % 16 == 0 && value_row_stride % 16 == 0;
+  return launch_append(a, dtype == NVFP4_BF16, mode, vec256, static_cast<cudaStream_t>(stream));
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_dequantize_paged(
+    nvfp4_paged_cache k_cache, nvfp4_paged_cache v_cache, int32_t page_size,
+    int32_t num_kv_heads, int32_t head_dim, int32_t kv_layout, const void* block_tables,
+    int32_t table_dtype, int32_t max_pages_per_request, const int32_t* seq_lens,
+    int32_t batch_size, const float* k_scale, const float* v_scale, void* output_k,
+    void* output_v, int32_t out_dtype, int32_t max_seq_len, int32_t* dev_status,
+    void* stream) {
+  clear_error();
+  const char* fn = "nvfp4_dequantize_paged";
+  if (nvfp4_status st = check_geometry(fn, page_size, num_kv_heads, head_dim, kv_layout)) return st;
+  if (out_dtype != NVFP4_F16 && out_dtype != NVFP4_BF16)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_dequantize_paged: out_dtype must be NVFP4_F16 or NVFP4_BF16");
+  if (table_dtype != NVFP4_I32 && table_dtype != NVFP4_I64)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_dequantize_paged: table_dtype must be NVFP4_I32 or NVFP4_I64");
+  if (batch_size < 0 || max_seq_len < 0 || max_pages_per_request < 0)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_dequantize_paged: negative size");
+  if (nvfp4_status st = check_cache(fn, "k_cache", k_cache, page_size, num_kv_heads, head_dim)) return st;
+  if (nvfp4_status st = check_cache(fn, "v_cache", v_cache, page_size, num_kv_heads, head_dim)) return st;
+  if (batch_size == 0 || max_seq_len == 0) return NVFP4_OK;
+  if (batch_size > kMaxScanBatch)
+    return fail(NVFP4_ERR_UNSUPPORTED, "nvfp4_dequantize_paged: batch_size above 16384");
+  if (!block_tables || !seq_lens || !k_scale || !v_scale || !output_k || !output_v)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_dequantize_paged: null device pointer");
+  if (!aligned(output_k, 16) || !aligned(output_v, 16) || !aligned(k_scale, 4) || !aligned(v_scale, 4))
+    return fail(NVFP4_ERR_ALIGNMENT, "nvfp4_dequantize_paged: outputs must be 16-byte aligned");
+  DequantArgs a{};
+  a.kc = k_cache;
+  a.vc = v_cache;
+  a.ps = page_size;
+  a.H = num_kv_heads;
+  a.D = head_dim;
+  a.nb = head_dim / 16;
+  a.layout = kv_layout;
+  a.div_row_blocks = make_div(static_cast<int64_t>(num_kv_heads) * a.nb);
+  a.div_nb = make_div(a.nb);
+  a.block_tables = block_tables;
+  a.max_pages = max_pages_per_request;
+  a.seq_lens = seq_lens;
+  a.B = batch_size;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.out_k = static_cast<uint8_t*>(output_k);
+  a.out_v = static_cast<uint8_t*>(output_v);
+  a.L = max_seq_len;
+  a.status = dev_status;
+  const bool vec256 = aligned(output_k, 32) && aligned(output_v, 32);
+  return launch_dequant(a, out_dtype == NVFP4_BF16, table_dtype == NVFP4_I64, vec256,
+                        static_cast<cudaStream_t>(stream));
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_materialize_fp8_out_pages(int32_t batch_size, int32_t max_kv_len,
+                                                          int32_t page_size, int64_t num_pages,
+                                                          int64_t* out_num_pages,
+                                                          int32_t* max_pages_per_seq) {
+  clear_error();
+  if (batch_size < 0 || max_kv_len < 0 || page_size < 1)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materialize_fp8_out_pages: bad size");
+  const int64_t mpps = (static_cast<int64_t>(max_kv_len) + page_size - 1) / page_size;
+  const int64_t n = num_pages >= 0 ? num_pages : static_cast<int64_t>(batch_size) * mpps;
+  if (out_num_pages) *out_num_pages = n + 1;
+  if (max_pages_per_seq) *max_pages_per_seq = static_cast<int32_t>(mpps);
+  return NVFP4_OK;
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_materialize_fp8(
+    nvfp4_paged_cache k_cache, nvfp4_paged_cache v_cache, int32_t page_size,
+    int32_t num_kv_heads, int32_t head_dim, int32_t kv_layout, const int32_t* block_tables,
+    int32_t max_num_pages, int32_t uses_shared_paged_kv_idx, const int32_t* seq_lens,
+    int32_t batch_size, int32_t max_kv_len, const int32_t* kv_page_indptr, int64_t num_pages,
+    uint8_t* out, int64_t out_num_pages, int32_t* fp8_block_tables,
+    int32_t zero_fp8_block_tables, int32_t* dev_status, void* stream) {
+  clear_error();
+  const char* fn = "nvfp4_materialize_fp8";
+  if (nvfp4_status st = check_geometry(fn, page_size, num_kv_heads, head_dim, kv_layout)) return st;
+  if (head_dim % 64 != 0) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materialize_fp8: head_dim must be divisible by 64");
+  if (page_size % 4 != 0) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materialize_fp8: page_size must be divisible by 4");
+  if (batch_size < 0 || max_kv_len < 0 || max_num_pages < 0)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materialize_fp8: negative size");
+  if (nvfp4_status st = check_cache(fn, "k_cache", k_cache, page_size, num_kv_heads, head_dim)) return st;
+  if (nvfp4_status st = check_cache(fn, "v_cache", v_cache, page_size, num_kv_heads, head_dim)) return st;
+  if (!aligned(k_cache.sf, 2) || !aligned(v_cache.sf, 2) || k_cache.sf_page_stride % 2 != 0 ||
+      v_cache.sf_page_stride % 2 != 0)
+    return fail(NVFP4_ERR_ALIGNMENT, "nvfp4_materialize_fp8: scale caches must be 2-byte aligned with even page strides");
+  const int64_t mpps = (static_cast<int64_t>(max_kv_len) + page_size - 1) / page_size;
+  if (max_num_pages < mpps)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materialize_fp8: block_tables needs at least ceil(max_kv_len / page_size) columns");
+  int64_t n = static_cast<int64_t>(batch_size) * mpps;
+  if (kv_page_indptr) {
+    if (num_pages < 0) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materialize_fp8: kv_page_indptr requires num_pages");
+    n = num_pages;
+  }
+  if (out_num_pages < n + 1)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materialize_fp8: out needs at least num_pages + 1 pages");
+  if (!out) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materialize_fp8: out is null");
+  if (!aligned(out, 32)) return fail(NVFP4_ERR_ALIGNMENT, "nvfp4_materialize_fp8: out must be 32-byte aligned");
+  if (batch_size > kMaxScanBatch)
+    return fail(NVFP4_ERR_UNSUPPORTED, "nvfp4_materialize_fp8: batch_size above 16384");
+  if (batch_size > 0 && (!block_tables || !seq_lens || !fp8_block_tables))
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materialize_fp8: null device pointer");
+  if (mpps > INT32_MAX || n + 1 > (int64_t(1) << 31))
+    return fail(NVFP4_ERR_UNSUPPORTED, "nvfp4_materialize_fp8: page counts above 2^31");
+  MaterializeArgs a{};
+  a.kc = k_cache;
+  a.vc = v_cache;
+  a.ps = page_size;
+  a.H = num_kv_heads;
+  a.D = head_dim;
+  a.layout = kv_layout;
+  a.div_page_chunks = make_div(static_cast<int64_t>(page_size) * (head_dim / 32));
+  a.div_row_chunks = make_div(head_dim / 32);
+  a.div_mpps = make_div(mpps > 0 ? mpps : 1);
+  a.block_tables = block_tables;
+  a.max_num_pages = max_num_pages;
+  a.shared = uses_shared_paged_kv_idx ? 1 : 0;
+  a.seq_lens = seq_lens;
+  a.B = batch_size;
+  a.mpps = static_cast<int32_t>(mpps);
+  a.kv_page_indptr = kv_page_indptr;
+  a.out = out;
+  a.out_num_pages = out_num_pages;
+  a.tables = fp8_block_tables;
+  a.zero_tables = zero_fp8_block_tables ? 1 : 0;
+  a.status = dev_status;
+  if (batch_size == 0) {
+    // nothing active: the copy is just its zero page
+    const size_t bytes = static_cast<size_t>(2) * num_kv_heads * page_size * head_dim;
+    const cudaError_t e = cudaMemsetAsync(out, 0, bytes, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, std::string("cudaMemsetAsync: ") + cudaGetErrorString(e));
+    return NVFP4_OK;
+  }
+  return launch_materialize(a, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

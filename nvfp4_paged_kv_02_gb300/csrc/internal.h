@@ -1,0 +1,102 @@
+// internal.h -- host-side declarations shared by the translation units of libnvfp4kv.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+
+#include "../../include/nvfp4kv.h"
+#include "device.cuh"
+
+#define NVFP4_EXPORT __attribute__((visibility("default")))
+
+namespace nvfp4 {
+
+// Per-thread error text behind nvfp4_last_error_string().
+void set_error(const std::string& msg);
+void clear_error();
+nvfp4_status fail(nvfp4_status code, const std::string& msg);
+// Check the launch that was just enqueued.
+nvfp4_status check_launch(const char* what);
+
+// Streaming multiprocessors of the current device.
+int sm_count();
+// Resident CTAs per SM for `kernel` at `threads` threads and `smem` dynamic bytes
+// (cached per kernel and device).
+int blocks_per_sm(const void* kernel, int threads, size_t smem);
+
+// Largest batch the page-scan kernels keep in shared memory (one int32 per request).
+constexpr int kMaxScanBatch = 16384;
+
+// ---- append ------------------------------------------------------------------------------
+struct AppendArgs {
+  const uint8_t* k;
+  const uint8_t* v;
+  int64_t k_row_bytes;
+  int64_t v_row_bytes;
+  int64_t nnz;
+  int32_t H, D, nb;
+  Div div_nb, div_H, div_ps;
+  const int32_t* batch_indices;
+  const int32_t* positions;
+  nvfp4_paged_cache kc, vc;
+  int32_t ps;
+  int32_t layout;
+  const int32_t* kv_indices;
+  int64_t num_kv_indices;
+  const int32_t* kv_indptr;
+  const int32_t* kv_last_page_len;
+  int32_t batch_size;
+  float gs[2];
+  float cap_a;
+  int32_t* status;
+};
+// mode: 0 standard NVFP4; 1/2 4over6 binary32 MAE/MSE; 3/4 4over6 binary16 MAE/MSE.
+nvfp4_status launch_append(const AppendArgs& a, bool bf16, int mode, bool vec256,
+                           cudaStream_t stream);
+
+// ---- dequantize --------------------------------------------------------------------------
+struct DequantArgs {
+  nvfp4_paged_cache kc, vc;
+  int32_t ps, H, D, nb, layout;
+  Div div_row_blocks, div_nb;
+  const void* block_tables;
+  int64_t max_pages;
+  const int32_t* seq_lens;
+  int32_t B;
+  const float* k_scale;
+  const float* v_scale;
+  uint8_t* out_k;
+  uint8_t* out_v;
+  int32_t L;
+  int32_t* status;
+};
+nvfp4_status launch_dequant(const DequantArgs& a, bool out_bf16, bool bt64, bool vec256,
+                            cudaStream_t stream);
+
+// ---- materialize -------------------------------------------------------------------------
+struct MaterializeArgs {
+  nvfp4_paged_cache kc, vc;
+  int32_t ps, H, D, layout;
+  Div div_page_chunks, div_row_chunks, div_mpps;
+  const int32_t* block_tables;
+  int64_t max_num_pages;
+  int32_t shared;
+  const int32_t* seq_lens;
+  int32_t B;
+  int32_t mpps;
+  const int32_t* kv_page_indptr;
+  uint8_t* out;
+  int64_t out_num_pages;
+  int32_t* tables;
+  int32_t zero_tables;
+  int32_t* status;
+};
+nvfp4_status launch_materialize(const MaterializeArgs& a, cudaStream_t stream);
+
+// ---- global scale ------------------------------------------------------------------------
+nvfp4_status launch_global_scale(const void* x, bool bf16, int64_t numel, float denom,
+                                 float* out, cudaStream_t stream);
+
+}  // namespace nvfp4

@@ -1,0 +1,150 @@
+// materialize.cu -- active pages of a paged NVFP4 cache -> FP8 E4M3 copy.
+//
+// FlashInfer "nvfp4_kv_materialize_fp8" (parameters, returns, note) and
+// "NVFP4KVMaterializer.run" ("flashinfer.quantization" index): request b's page j goes to
+// output page kv_page_indptr[b] + j + 1 (b * max_pages_per_seq + j + 1 by default) of a
+// [num_pages + 1, 2, H, page_size, D] float8_e4m3fn copy whose page 0 is zero; only E2M1
+// value x E4M3 block scale is applied (exact in binary16), rounded to E4M3 with saturation
+// at 448; fp8_block_tables[b, j] holds the output page.
+//
+// Persistent CTAs walk a flat list of (active page, K|V) items from a shared-memory scan of
+// the request lengths. An item converts H * page_size * D elements; thread k handles the
+// 32-element chunk k of the output half page (16 code bytes + 2 scale bytes in, one
+// 32-byte store out). With HND input, chunk k is also the k-th 16-byte chunk of the input
+// page, so both streams are contiguous.
+#include "internal.h"
+#include "scan.cuh"
+
+namespace nvfp4 {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;
+
+__device__ __forceinline__ uint32_t fp8x2(uint32_t h2, uint32_t S2) {
+  return e4m3x2_from_f16x2(hmul2_rn(h2, S2));
+}
+
+// 16 code bytes (32 elements, two blocks) with scale bytes s0, s1 -> 32 E4M3 bytes.
+__device__ __forceinline__ U32x8 convert_chunk(uint4 c, uint32_t s01) {
+  const uint32_t s0 = s01 & 0xFFu, s1 = (s01 >> 8) & 0xFFu;
+  const uint32_t S0 = f16x2_from_e4m3x2(s0 | (s0 << 8));
+  const uint32_t S1 = f16x2_from_e4m3x2(s1 | (s1 << 8));
+  const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+  U32x8 o;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t h0, h1, h2, h3;
+    f16x2x4_from_e2m1x8(cw[q], h0, h1, h2, h3);
+    const uint32_t S = q < 2 ? S0 : S1;
+    o.w[2 * q] = fp8x2(h0, S) | (fp8x2(h1, S) << 16);
+    o.w[2 * q + 1] = fp8x2(h2, S) | (fp8x2(h3, S) << 16);
+  }
+  return o;
+}
+
+__global__ void __launch_bounds__(kThreads) materialize_kernel(const MaterializeArgs a) {
+  extern __shared__ int32_t s_cum[];
+  const int32_t ps = a.ps;
+  const int32_t mpps = a.mpps;
+  block_inclusive_scan(s_cum, a.B, [&](int32_t b) {
+    const int32_t len = __ldg(a.seq_lens + b);
+    int32_t n = len > 0 ? static_cast<int32_t>((static_cast<int64_t>(len) + ps - 1) / ps) : 0;
+    if (n > mpps) {
+      flag(a.status, NVFP4_DEV_LEN_CLAMPED);
+      n = mpps;
+    }
+    return n;
+  });
+  const int32_t pages = s_cum[a.B - 1];
+  const int64_t half_page = static_cast<int64_t>(a.H) * ps * a.D;  // bytes of K or V
+  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t gstep = static_cast<int64_t>(gridDim.x) * blockDim.x;
+
+  // page 0 of the copy is zero
+  for (int64_t q = gtid; q < 2 * half_page / 16; q += gstep)
+    reinterpret_cast<uint4*>(a.out)[q] = make_uint4(0, 0, 0, 0);
+
+  // page table: active entries, and zero padding in the functional form
+  const int64_t entries = static_cast<int64_t>(a.B) * mpps;
+  for (int64_t e = gtid; e < entries; e += gstep) {
+    const int32_t b = static_cast<int32_t>(div_q(e, a.div_mpps));
+    const int32_t j = static_cast<int32_t>(e - static_cast<int64_t>(b) * mpps);
+    const int32_t n = s_cum[b] - (b > 0 ? s_cum[b - 1] : 0);
+    if (j < n) {
+      const int64_t base = a.kv_page_indptr ? __ldg(a.kv_page_indptr + b)
+                                            : static_cast<int64_t>(b) * mpps;
+      a.tables[e] = static_cast<int32_t>(base + j + 1);
+    } else if (a.zero_tables) {
+      a.tables[e] = 0;
+    }
+  }
+
+  const int32_t row_chunks = a.D / 32;
+  const int32_t chunks = a.H * ps * row_chunks;
+  for (int64_t item = blockIdx.x; item < 2 * static_cast<int64_t>(pages); item += gridDim.x) {
+    const int kv = static_cast<int>(item & 1);
+    const int32_t pi = static_cast<int32_t>(item >> 1);
+    const int32_t b = scan_find(s_cum, a.B, pi);
+    const int32_t j = pi - (b > 0 ? s_cum[b - 1] : 0);
+    const int64_t tcol = a.shared ? static_cast<int64_t>(b) * a.max_num_pages + j
+                                  : (static_cast<int64_t>(b) * 2 + kv) * a.max_num_pages + j;
+    const int64_t page = __ldg(a.block_tables + tcol);
+    const int64_t base = a.kv_page_indptr ? __ldg(a.kv_page_indptr + b)
+                                          : static_cast<int64_t>(b) * mpps;
+    const int64_t o = base + j + 1;
+    const nvfp4_paged_cache& c = kv ? a.vc : a.kc;
+    if (page < 0 || page >= c.num_pages) {
+      if (threadIdx.x == 0) flag(a.status, NVFP4_DEV_BAD_PAGE);
+      continue;
+    }
+    if (o < 1 || o >= a.out_num_pages) {
+      if (threadIdx.x == 0) flag(a.status, NVFP4_DEV_BAD_OUT_PAGE);
+      continue;
+    }
+    const uint8_t* __restrict__ pd = c.data + page * c.data_page_stride;
+    const uint8_t* __restrict__ psf = c.sf + page * c.sf_page_stride;
+    uint8_t* __restrict__ dst = a.out + (o * 2 + kv) * half_page;
+
+    for (int32_t k0 = threadIdx.x; k0 < chunks; k0 += kThreads * kUnroll) {
+      uint4 cv[kUnroll];
+      uint32_t sv[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int32_t k = k0 + u * kThreads;
+        if (k < chunks) {
+          int32_t off = k;  // HND: chunk k of the output is chunk k of the input page
+          if (a.layout == NVFP4_NHD) {
+            const int32_t h = static_cast<int32_t>(div_q(k, a.div_page_chunks));
+            const int32_t rem = k - h * (ps * row_chunks);
+            const int32_t slot = static_cast<int32_t>(div_q(rem, a.div_row_chunks));
+            off = (slot * a.H + h) * row_chunks + (rem - slot * row_chunks);
+          }
+          cv[u] = __ldg(reinterpret_cast<const uint4*>(pd) + off);
+          sv[u] = __ldg(reinterpret_cast<const uint16_t*>(psf) + off);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int32_t k = k0 + u * kThreads;
+        if (k < chunks) st_256(dst + static_cast<int64_t>(k) * 32, convert_chunk(cv[u], sv[u]));
+      }
+    }
+  }
+}
+
+}  // namespace
+
+nvfp4_status launch_materialize(const MaterializeArgs& a, cudaStream_t stream) {
+  const auto kern = materialize_kernel;
+  const size_t smem = static_cast<size_t>(a.B) * sizeof(int32_t);
+  if (smem > 48 * 1024) {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(smem));
+  }
+  const int grid = sm_count() * blocks_per_sm(reinterpret_cast<const void*>(kern), kThreads, smem);
+  kern<<<grid, kThreads, smem, stream>>>(a);
+  return check_launch("nvfp4_materialize_fp8");
+}
+
+}  // namespace nvfp4
