@@ -203,9 +203,10 @@ class Step:
         rec(5)
 
 
-def make_workload(name: str, dev: torch.device) -> W.Workload:
+def make_workload(name: str, dev: torch.device, batch: int = 256,
+                  pool_gb: float = W.LARGE_POOL_BYTES / 1e9) -> W.Workload:
     if name == "large_pool":
-        return W.large_pool(device=str(dev))
+        return W.large_pool(device=str(dev), B=batch, pool_bytes=pool_gb * 1e9)
     return W.NAMED[name]()
 
 
@@ -293,6 +294,9 @@ def main():
                     choices=["large_pool", "decode", "prefill", "materialize", "tiny"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--ref-requests", type=int, default=4)
+    ap.add_argument("--batch", type=int, default=256, help="large_pool: requests")
+    ap.add_argument("--pool-gb", type=float, default=W.LARGE_POOL_BYTES / 1e9,
+                    help="large_pool: pool size (K+V codes and scales), GB")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -306,7 +310,8 @@ def main():
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     if args.impl == "reference":
         if rank == 0:
-            w = make_workload(args.workload, torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu"))
+            w = make_workload(args.workload, torch.device("cuda", local) if torch.cuda.is_available()
+                              else torch.device("cpu"), args.batch, args.pool_gb)
             reference_arm(args, w)
         if world > 1:
             import torch.distributed as dist
@@ -319,7 +324,7 @@ def main():
     dev = torch.device("cuda", local)
     import nvfp4_paged_kv_02_gb300 as nv
     nv.load()
-    w = make_workload(args.workload, dev)
+    w = make_workload(args.workload, dev, args.batch, args.pool_gb)
     step = Step(w, dev)
     nbytes, ntok = op_bytes(w, active_pages(w))
     total_bytes = sum(nbytes.values())
