@@ -232,9 +232,10 @@ static double tree16_f16(double t[16]) {
 /* Reconstruction error of a candidate ([P4]: "quantizes the block with both, dequantizes
  * both"). Reading: the element error is x - e2m1(q)*S*gs computed exactly and rounded once
  * (a fused multiply-add) -- "exactly in fp32"; the summed term is |e| (MAE) or e*e rounded
- * (MSE). With fast math ([P4] err_use_fast_math) every quantity is binary16: x and gs are
- * rounded to binary16, e2m1(q)*S is exact in binary16, and e, e*e and each partial sum are
- * rounded to binary16. */
+ * (MSE). With fast math ([P4] err_use_fast_math: the error "in fp16") every step is a
+ * binary16 operation: x and gs are rounded to binary16, the block's decode factor is
+ * sg = RN16(S * gs_h), the element error is e = RN16(x_h - e2m1(q) * sg) (fused), and e*e
+ * and each partial sum are rounded to binary16. */
 static double block_error(const float x[16], const uint32_t q[16], uint32_t s, float gs,
                           const oracle_recipe* r) {
   double S = oracle_e4m3_decode(s);
@@ -250,10 +251,11 @@ static double block_error(const float x[16], const uint32_t q[16], uint32_t s, f
   }
   double t[16];
   double gh = f16_round((double)gs);
+  double sg = f16_round(S * gh); /* S*gh is exact in double */
   for (int i = 0; i < 16; ++i) {
     double xh = f16_round((double)x[i]);
-    double w = oracle_e2m1_decode(q[i]) * S; /* exact in binary16 */
-    double e = f16_round(fma(-w, gh, xh));   /* exact in double before the one rounding */
+    double v = oracle_e2m1_decode(q[i]);
+    double e = f16_round(fma(-v, sg, xh)); /* exact in double before the one rounding */
     t[i] = mse ? f16_round(e * e) : fabs(e);
   }
   return tree16_f16(t);
