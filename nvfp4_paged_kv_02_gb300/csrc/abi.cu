@@ -208,6 +208,7 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_append_paged(
   a.gs[0] = k_scale;
   a.gs[1] = v_scale;
   a.cap_a = nvfp4_e4m3_max(recipe);
+  a.neg_zero = 0x80000000u;
   a.status = dev_status;
   int mode = 0;
   if (recipe) mode = 1 + (recipe->err_mode == NVFP4_ERR_MSE ? 1 : 0) + (recipe->err_use_fast_math ? 2 : 0);

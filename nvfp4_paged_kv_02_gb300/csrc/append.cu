@@ -11,14 +11,20 @@
 // Per block and candidate scale byte s (S = E4M3 value, gs = global decode scale):
 //   inv = 1 / (S * gs)      (binary32 reciprocal; 0 when S*gs is 0; at most FLT_MAX)
 //   q_i = E2M1_RNE_satfinite(x_i * inv)
-// The 256 possible `inv` per tensor are computed once per CTA into shared memory.
-// Standard NVFP4: s = E4M3(min(amax / (6 gs), e4m3_max)).
+// Standard NVFP4: s = E4M3(min(amax / (6 gs), e4m3_max)); the quotient is the correctly
+// rounded one, from a precomputed reciprocal of 6 gs (see div_rn_with_rcp).
 // 4over6: s_B = E4M3(min(amax / (4 gs), 448)) as well; each candidate's error sums, over the
-// block, |e_i| (MAE) or e_i^2 (MSE) with e_i = x_i - e2m1(q_i) * S * gs, rounded once
-// (binary32 FMA) -- or, with fast math, the whole error in binary16 (x, gs rounded to
-// binary16; e2m1 * S exact in binary16; fused multiply-subtract; squares and sums rounded to
-// binary16). The sum runs over a fixed halving tree: t[i] += t[i+8], t[i+4], t[i+2], t[i+1].
-// B is kept only when its error is strictly smaller.
+// block, |e_i| (MAE) or e_i^2 (MSE):
+//   binary32 error: e_i = x_i - e2m1(q_i) * S * gs, rounded once (e2m1 * S is exact in
+//                   binary16, the rest is one fused multiply-add);
+//   binary16 error: e_i = RN16(x_h - e2m1(q_i) * sg) with x_h = RN16(x_i) and
+//                   sg = RN16(S * RN16(gs)); squares and sums rounded to binary16.
+// The sum runs over a fixed halving tree: t[i] += t[i+8], t[i+4], t[i+2], t[i+1], which
+// is exactly the order of the packed two-lane adds. B is kept only when its error is
+// strictly smaller.
+//
+// Per-CTA shared tables, indexed by scale byte: 1/(S*gs) (both tensors), (S, S) as half2,
+// and -sg as half2 (both tensors).
 #include <cfloat>
 
 #include "internal.h"
@@ -27,6 +33,31 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kThreads = 256;
+
+// Per-tensor constants for one block quantization.
+struct TensorConsts {
+  float gs;       // global decode scale
+  float g6, r6;   // fp32(6 gs) and its reciprocal
+  float g4, r4;   // 4 gs and its reciprocal
+  bool exact_rcp; // both divisors and reciprocals are normal: use div_rn_with_rcp
+};
+
+__device__ __forceinline__ TensorConsts make_consts(float gs) {
+  TensorConsts c;
+  c.gs = gs;
+  c.g6 = __fmul_rn(6.0f, gs);
+  c.g4 = __fmul_rn(4.0f, gs);
+  c.r6 = __frcp_rn(c.g6);
+  c.r4 = __frcp_rn(c.g4);
+  const float lo = FLT_MIN, hi = FLT_MAX;
+  c.exact_rcp = c.g6 >= lo && c.g6 <= hi && c.g4 >= lo && c.r6 >= lo && c.r6 <= hi &&
+                c.r4 >= lo && c.r4 <= hi;
+  return c;
+}
+
+__device__ __forceinline__ float quotient(float a, float b, float rb, bool exact_rcp) {
+  return exact_rcp ? div_rn_with_rcp(a, b, rb) : __fdiv_rn(a, b);
+}
 
 template <bool BF16>
 __device__ __forceinline__ void unpack16(const U32x8& in, float x[16]) {
@@ -42,59 +73,116 @@ __device__ __forceinline__ void unpack16(const U32x8& in, float x[16]) {
   }
 }
 
-// Codes of the block for element multiplier `inv`: two words of four code bytes each.
-__device__ __forceinline__ void encode16(const float x[16], float inv, uint32_t& c0,
-                                         uint32_t& c1) {
-  float y[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(x[i], inv);
-  c0 = e2m1x8_from_f32(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
-  c1 = e2m1x8_from_f32(y[8], y[9], y[10], y[11], y[12], y[13], y[14], y[15]);
+// Four element pairs (x[0..7]) with multiplier inv: the four code bytes, and the decoded
+// values e2m1(q) as four half2.
+__device__ __forceinline__ uint32_t encode8(const float* x, float inv, uint32_t v[4]) {
+  uint32_t code;
+  asm("{\n\t"
+      ".reg .b64 ip, p0, p1, p2, p3;\n\t"
+      ".reg .f32 y0, y1, y2, y3, y4, y5, y6, y7;\n\t"
+      ".reg .b8 q0, q1, q2, q3;\n\t"
+      "mov.b64 ip, {%5, %5};\n\t"
+      "mov.b64 p0, {%6, %7};\n\t"
+      "mov.b64 p1, {%8, %9};\n\t"
+      "mov.b64 p2, {%10, %11};\n\t"
+      "mov.b64 p3, {%12, %13};\n\t"
+      "mul.rn.f32x2 p0, p0, ip;\n\t"
+      "mul.rn.f32x2 p1, p1, ip;\n\t"
+      "mul.rn.f32x2 p2, p2, ip;\n\t"
+      "mul.rn.f32x2 p3, p3, ip;\n\t"
+      "mov.b64 {y0, y1}, p0;\n\t"
+      "mov.b64 {y2, y3}, p1;\n\t"
+      "mov.b64 {y4, y5}, p2;\n\t"
+      "mov.b64 {y6, y7}, p3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q0, y1, y0;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q1, y3, y2;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q2, y5, y4;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q3, y7, y6;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, q0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, q1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, q2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %4, q3;\n\t"
+      "mov.b32 %0, {q0, q1, q2, q3};\n\t"
+      "}"
+      : "=r"(code), "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+      : "f"(inv), "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]),
+        "f"(x[7]));
+  return code;
 }
 
-// e2m1(q) * S as eight half2 (exact: at most 6 significant bits, inside binary16's range).
-__device__ __forceinline__ void scaled_codes(uint32_t c0, uint32_t c1, uint32_t S2,
-                                             uint32_t w[8]) {
-  f16x2x4_from_e2m1x8(c0, w[0], w[1], w[2], w[3]);
-  f16x2x4_from_e2m1x8(c1, w[4], w[5], w[6], w[7]);
-#pragma unroll
-  for (int k = 0; k < 8; ++k) w[k] = hmul2_rn(w[k], S2);
+// Codes of a block without the decoded values (standard NVFP4).
+__device__ __forceinline__ uint32_t codes8(const float* x, float inv) {
+  uint32_t code;
+  asm("{\n\t"
+      ".reg .b64 ip, p0, p1, p2, p3;\n\t"
+      ".reg .f32 y0, y1, y2, y3, y4, y5, y6, y7;\n\t"
+      ".reg .b8 q0, q1, q2, q3;\n\t"
+      "mov.b64 ip, {%1, %1};\n\t"
+      "mov.b64 p0, {%2, %3};\n\t"
+      "mov.b64 p1, {%4, %5};\n\t"
+      "mov.b64 p2, {%6, %7};\n\t"
+      "mov.b64 p3, {%8, %9};\n\t"
+      "mul.rn.f32x2 p0, p0, ip;\n\t"
+      "mul.rn.f32x2 p1, p1, ip;\n\t"
+      "mul.rn.f32x2 p2, p2, ip;\n\t"
+      "mul.rn.f32x2 p3, p3, ip;\n\t"
+      "mov.b64 {y0, y1}, p0;\n\t"
+      "mov.b64 {y2, y3}, p1;\n\t"
+      "mov.b64 {y4, y5}, p2;\n\t"
+      "mov.b64 {y6, y7}, p3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q0, y1, y0;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q1, y3, y2;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q2, y5, y4;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q3, y7, y6;\n\t"
+      "mov.b32 %0, {q0, q1, q2, q3};\n\t"
+      "}"
+      : "=r"(code)
+      : "f"(inv), "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]),
+        "f"(x[7]));
+  return code;
 }
 
-// Binary32 reconstruction error of one candidate.
+// One candidate with the binary32 error: codes c0, c1 and the error sum.
 template <bool MSE>
-__device__ __forceinline__ float error_f32(const float x[16], uint32_t c0, uint32_t c1,
-                                           uint32_t S2, float neg_gs) {
-  uint32_t w[8];
-  scaled_codes(c0, c1, S2, w);
-  float t[16];
+__device__ __forceinline__ float candidate_f32(const float x[16], float inv, uint32_t S2,
+                                               float neg_gs, uint64_t nz2, uint32_t& c0,
+                                               uint32_t& c1) {
+  uint32_t v[8];
+  c0 = encode8(x, inv, v);
+  c1 = encode8(x + 8, inv, v + 4);
+  uint64_t t[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    const float e0 = __fmaf_rn(f32_from_f16_lo(w[k]), neg_gs, x[2 * k]);
-    const float e1 = __fmaf_rn(f32_from_f16_hi(w[k]), neg_gs, x[2 * k + 1]);
-    t[2 * k] = MSE ? __fmul_rn(e0, e0) : fabsf(e0);
-    t[2 * k + 1] = MSE ? __fmul_rn(e1, e1) : fabsf(e1);
+    const uint32_t w = hmul2_rn(v[k], S2);  // e2m1 * S, exact
+    // the element error needs a true single rounding: scalar fused multiply-adds
+    const float e0 = __fmaf_rn(f32_from_f16_lo(w), neg_gs, x[2 * k]);
+    const float e1 = __fmaf_rn(f32_from_f16_hi(w), neg_gs, x[2 * k + 1]);
+    const uint64_t e = f32x2_pack(e0, e1);
+    t[k] = MSE ? fsq2_rn(e, nz2) : (e & 0x7FFFFFFF7FFFFFFFull);
   }
 #pragma unroll
-  for (int half = 8; half >= 1; half /= 2) {
-#pragma unroll
-    for (int i = 0; i < half; ++i) t[i] = __fadd_rn(t[i], t[i + half]);
-  }
-  return t[0];
+  for (int k = 0; k < 4; ++k) t[k] = fadd2_rn(t[k], t[k + 4]);
+  t[0] = fadd2_rn(t[0], t[2]);
+  t[1] = fadd2_rn(t[1], t[3]);
+  t[0] = fadd2_rn(t[0], t[1]);
+  float lo, hi;
+  f32x2_unpack(t[0], lo, hi);
+  return __fadd_rn(lo, hi);
 }
 
-// Binary16 ("fast math") reconstruction error of one candidate; returned widened to float.
+// One candidate with the binary16 error: codes c0, c1 and the error sum (as a float).
 template <bool MSE>
-__device__ __forceinline__ float error_f16(const uint32_t xh[8], uint32_t c0, uint32_t c1,
-                                           uint32_t S2, uint32_t neg_gh2) {
+__device__ __forceinline__ float candidate_f16(const float x[16], const uint32_t xh[8], float inv,
+                                               uint32_t neg_sg2, uint32_t nzh2, uint32_t& c0,
+                                               uint32_t& c1) {
   uint32_t t[8];
-  scaled_codes(c0, c1, S2, t);
+  c0 = encode8(x, inv, t);
+  c1 = encode8(x + 8, inv, t + 4);
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    const uint32_t e = hfma2_rn(t[k], neg_gh2, xh[k]);
-    t[k] = MSE ? hmul2_rn(e, e) : (e & 0x7FFF7FFFu);
+    const uint32_t e = hfma2_rn(t[k], neg_sg2, xh[k]);
+    t[k] = MSE ? hsq2_rn(e, nzh2) : (e & 0x7FFF7FFFu);
   }
-  // pairs hold elements (2k, 2k+1): pair k + pair k+4 is t[i] + t[i+8], and so on
 #pragma unroll
   for (int k = 0; k < 4; ++k) t[k] = hadd2_rn(t[k], t[k + 4]);
   t[0] = hadd2_rn(t[0], t[2]);
@@ -105,46 +193,50 @@ __device__ __forceinline__ float error_f16(const uint32_t xh[8], uint32_t c0, ui
   return __half2float(s);
 }
 
+struct Tables {
+  float inv[2][256];       // 1 / (S * gs) per tensor
+  uint32_t neg_sg2[2][256];  // (-RN16(S * RN16(gs))) in both halves, per tensor
+  uint32_t S2[256];        // (S, S) as half2
+};
+
 struct BlockOut {
   uint32_t c0, c1, s;
 };
 
 template <bool BF16, int MODE>
-__device__ __forceinline__ BlockOut quantize_block(const U32x8& in, float gs,
-                                                   const float* __restrict__ inv_tab,
-                                                   float cap_a, uint32_t neg_gh2) {
+__device__ __forceinline__ BlockOut quantize_block(const U32x8& in, const TensorConsts& tc,
+                                                   const Tables& tab, int kv, float cap_a,
+                                                   uint32_t nz) {
   float x[16];
   unpack16<BF16>(in, x);
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-  const float ra = fminf(__fdiv_rn(amax, __fmul_rn(6.0f, gs)), cap_a);
+  const float ra = fminf(quotient(amax, tc.g6, tc.r6, tc.exact_rcp), cap_a);
   BlockOut r;
   if (MODE == 0) {
     r.s = e4m3x2_from_f32(ra, 0.0f) & 0xFFu;
-    encode16(x, inv_tab[r.s], r.c0, r.c1);
+    const float inv = tab.inv[kv][r.s];
+    r.c0 = codes8(x, inv);
+    r.c1 = codes8(x + 8, inv);
     return r;
   }
-  const float rb = fminf(__fdiv_rn(amax, __fmul_rn(4.0f, gs)), 448.0f);
+  const float rb = fminf(quotient(amax, tc.g4, tc.r4, tc.exact_rcp), 448.0f);
   const uint32_t sab = e4m3x2_from_f32(ra, rb);
   const uint32_t sa = sab & 0xFFu, sb = sab >> 8;
   uint32_t a0, a1, b0, b1;
-  encode16(x, inv_tab[sa], a0, a1);
-  encode16(x, inv_tab[sb], b0, b1);
-  const uint32_t S2 = f16x2_from_e4m3x2(sab);
-  const uint32_t SA2 = __byte_perm(S2, 0, 0x1010);  // (S_A, S_A)
-  const uint32_t SB2 = __byte_perm(S2, 0, 0x3232);  // (S_B, S_B)
   float ea, eb;
   if (MODE == 1 || MODE == 2) {
-    const float neg_gs = -gs;
-    ea = error_f32<MODE == 2>(x, a0, a1, SA2, neg_gs);
-    eb = error_f32<MODE == 2>(x, b0, b1, SB2, neg_gs);
+    const uint64_t nz2 = (static_cast<uint64_t>(nz) << 32) | nz;
+    ea = candidate_f32<MODE == 2>(x, tab.inv[kv][sa], tab.S2[sa], -tc.gs, nz2, a0, a1);
+    eb = candidate_f32<MODE == 2>(x, tab.inv[kv][sb], tab.S2[sb], -tc.gs, nz2, b0, b1);
   } else {
     uint32_t xh[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) xh[k] = BF16 ? f16x2_from_f32(x[2 * k], x[2 * k + 1]) : in.w[k];
-    ea = error_f16<MODE == 4>(xh, a0, a1, SA2, neg_gh2);
-    eb = error_f16<MODE == 4>(xh, b0, b1, SB2, neg_gh2);
+    const uint32_t nzh2 = (nz >> 16) | nz;  // binary16 -0 in both halves
+    ea = candidate_f16<MODE == 4>(x, xh, tab.inv[kv][sa], tab.neg_sg2[kv][sa], nzh2, a0, a1);
+    eb = candidate_f16<MODE == 4>(x, xh, tab.inv[kv][sb], tab.neg_sg2[kv][sb], nzh2, b0, b1);
   }
   const bool take_b = eb < ea;
   r.c0 = take_b ? b0 : a0;
@@ -155,23 +247,24 @@ __device__ __forceinline__ BlockOut quantize_block(const U32x8& in, float gs,
 
 template <bool BF16, int MODE, bool VEC256>
 __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
-  __shared__ float s_inv[2][256];
+  __shared__ Tables tab;
   for (int s = threadIdx.x; s < 256; s += blockDim.x) {
-    const float S = f32_from_f16_lo(f16x2_from_e4m3x2(static_cast<uint32_t>(s)));
+    const uint32_t S2 = f16x2_from_e4m3x2(static_cast<uint32_t>(s) * 0x0101u);
+    const float S = f32_from_f16_lo(S2);
+    tab.S2[s] = S2;
 #pragma unroll
     for (int kv = 0; kv < 2; ++kv) {
       const float den = __fmul_rn(S, a.gs[kv]);
-      s_inv[kv][s] = den == 0.0f ? 0.0f : fminf(__frcp_rn(den), FLT_MAX);
+      tab.inv[kv][s] = den == 0.0f ? 0.0f : fminf(__frcp_rn(den), FLT_MAX);
+      const __half gh = __float2half_rn(a.gs[kv]);
+      const __half sg = __hmul_rn(__ushort_as_half(static_cast<unsigned short>(S2 & 0xFFFFu)), gh);
+      const uint32_t n = static_cast<uint32_t>(__half_as_ushort(sg)) ^ 0x8000u;
+      tab.neg_sg2[kv][s] = n | (n << 16);
     }
   }
   __syncthreads();
-
-  uint32_t neg_gh2[2];
-#pragma unroll
-  for (int kv = 0; kv < 2; ++kv) {
-    const uint32_t gh = __half_as_ushort(__float2half_rn(a.gs[kv])) ^ 0x8000u;
-    neg_gh2[kv] = gh | (gh << 16);
-  }
+  const TensorConsts tck = make_consts(a.gs[0]);
+  const TensorConsts tcv = make_consts(a.gs[1]);
 
   const int64_t total = a.nnz * a.H * a.nb;
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -215,7 +308,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
         continue;
       }
       const BlockOut q =
-          quantize_block<BF16, MODE>(kv ? xv : xk, a.gs[kv], s_inv[kv], a.cap_a, neg_gh2[kv]);
+          quantize_block<BF16, MODE>(kv ? xv : xk, kv ? tcv : tck, tab, kv, a.cap_a, a.neg_zero);
       uint8_t* dst = c.data + page * c.data_page_stride + r * (a.D / 2) + 8 * j;
       *reinterpret_cast<uint2*>(dst) = make_uint2(q.c0, q.c1);
       c.sf[page * c.sf_page_stride + r * a.nb + j] = static_cast<uint8_t>(q.s);

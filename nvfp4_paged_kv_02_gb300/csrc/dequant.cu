@@ -10,16 +10,18 @@
 // scan of the request lengths in shared memory. One item is a page's tokens x all heads:
 // its output is one contiguous run of ntok * H * D elements. Thread k of the item decodes
 // 16-element block k (8 code bytes + 1 scale byte) into a 32-byte store, so each warp
-// store covers 1 KB of contiguous output; four blocks per thread are loaded before any is
-// decoded to keep enough bytes in flight.
+// store covers 1 KB of contiguous output; up to eight blocks per thread are loaded before any
+// is decoded to keep enough bytes in flight.
 #include "internal.h"
 #include "scan.cuh"
 
 namespace nvfp4 {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kUnroll = 4;
+// 128-thread CTAs (about a dozen resident per SM) each load a whole 16-token page's blocks
+// per thread before decoding, so many pages' loads are in flight at once.
+constexpr int kThreads = 128;
+constexpr int kUnroll = 8;
 
 template <bool OUT_BF16>
 __device__ __forceinline__ U32x8 decode_block(uint2 codes, uint32_t s, float gs) {

@@ -119,6 +119,53 @@ __device__ __forceinline__ uint32_t hfma2_rn(uint32_t a, uint32_t b, uint32_t c)
   return r;
 }
 
+// ---- packed binary32 arithmetic (sm_100+ f32x2 forms; two lanes per instruction) -------
+
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f32x2_unpack(uint64_t p, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(p));
+}
+__device__ __forceinline__ uint64_t fmul2_rn(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fadd2_rn(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// Squares written as a fused multiply-add whose addend `nz` is -0 at run time:
+// RN(a*a + -0) == RN(a*a), one rounding. The compiler cannot see that the addend is -0, so
+// it can neither turn the FMA back into a multiply nor contract it into a following add.
+// (ptxas was seen to fuse a packed mul.rn.f32x2 -- and an fma with a literal -0 addend --
+// into the next packed add despite the .rn modifier and -fmad=false, which changes the
+// rounding of an error sum.)
+__device__ __forceinline__ uint64_t fsq2_rn(uint64_t a, uint64_t nz) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %1, %2;" : "=l"(r) : "l"(a), "l"(nz));
+  return r;
+}
+__device__ __forceinline__ uint32_t hsq2_rn(uint32_t a, uint32_t nz) {
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %1, %2;" : "=r"(r) : "r"(a), "r"(nz));
+  return r;
+}
+
+// Correctly rounded a / b from a precomputed rb = RN(1/b): q0 = a*rb, the residual
+// a - q0*b is exact in a fused multiply-add, and q0 + residual*rb rounds to RN(a/b)
+// (Markstein's theorem) for normal b and normal a/b.
+__device__ __forceinline__ float div_rn_with_rcp(float a, float b, float rb) {
+  const float q0 = __fmul_rn(a, rb);
+  const float r = __fmaf_rn(-q0, b, a);
+  return __fmaf_rn(r, rb, q0);
+}
+
 // ---- memory access ----------------------------------------------------------------------
 
 struct U32x8 {

@@ -50,6 +50,7 @@ struct AppendArgs {
   int32_t batch_size;
   float gs[2];
   float cap_a;
+  uint32_t neg_zero;  // 0x80000000 (-0.0f), passed at run time for fsq2_rn / hsq2_rn
   int32_t* status;
 };
 // mode: 0 standard NVFP4; 1/2 4over6 binary32 MAE/MSE; 3/4 4over6 binary16 MAE/MSE.

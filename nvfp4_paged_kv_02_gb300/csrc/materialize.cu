@@ -18,7 +18,9 @@
 namespace nvfp4 {
 namespace {
 
-constexpr int kThreads = 256;
+// 128-thread CTAs (about a dozen resident per SM): each thread loads its four chunks of a
+// 16-token page before converting, and many pages are in flight per SM.
+constexpr int kThreads = 128;
 constexpr int kUnroll = 4;
 
 __device__ __forceinline__ uint32_t fp8x2(uint32_t h2, uint32_t S2) {
