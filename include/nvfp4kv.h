@@ -79,6 +79,7 @@ typedef int32_t nvfp4_status;
 #define NVFP4_DEV_BAD_PAGE 4      /* a physical page index outside [0, num_pages) */
 #define NVFP4_DEV_LEN_CLAMPED 8   /* a sequence length beyond the output extent, clamped */
 #define NVFP4_DEV_BAD_OUT_PAGE 16 /* materialize: output page index outside the workspace */
+#define NVFP4_DEV_TIMEOUT 32      /* a pipeline wait gave up (the kernel stopped early) */
 
 /* A 4over6 recipe ("NVFP44Over6Config"; "NVFP4 4over6 Recipes" section). A NULL recipe
  * pointer means standard NVFP4 (4over6 off), as None does in the pages' kernel drivers.

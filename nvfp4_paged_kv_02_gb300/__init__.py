@@ -40,6 +40,7 @@ F16, BF16 = 0, 1
 NHD, HND = 0, 1
 I32, I64 = 0, 1
 DEV_BAD_BATCH, DEV_BAD_POSITION, DEV_BAD_PAGE, DEV_LEN_CLAMPED, DEV_BAD_OUT_PAGE = 1, 2, 4, 8, 16
+DEV_TIMEOUT = 32
 
 
 class NVFP4KVError(RuntimeError):

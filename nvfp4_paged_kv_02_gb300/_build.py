@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libnvfp4kv.so")
 SOURCES = ["abi.cu", "append.cu", "dequant.cu", "materialize.cu", "global_scale.cu"]
-HEADERS = ["device.cuh", "internal.h", "scan.cuh"]
+HEADERS = ["device.cuh", "internal.h", "scan.cuh", "pipeline.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-fmad=false", "--extended-lambda",
               "-Xcompiler", "-fPIC,-fvisibility=hidden,-O2", "-I", os.path.join(ROOT, "include")]

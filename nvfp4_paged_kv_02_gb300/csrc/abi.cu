@@ -194,6 +194,7 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_append_paged(
   a.div_nb = make_div(a.nb);
   a.div_H = make_div(num_kv_heads);
   a.div_ps = make_div(page_size);
+  a.div_row_blocks = make_div(static_cast<int64_t>(num_kv_heads) * a.nb);
   a.batch_indices = batch_indices;
   a.positions = positions;
   a.kc = k_cache;

@@ -28,6 +28,7 @@
 #include <cfloat>
 
 #include "internal.h"
+#include "pipeline.cuh"
 
 namespace nvfp4 {
 namespace {
@@ -71,6 +72,35 @@ __device__ __forceinline__ void unpack16(const U32x8& in, float x[16]) {
       x[2 * k + 1] = f32_from_f16_hi(in.w[k]);
     }
   }
+}
+
+// max |x| of the block, exactly, from the packed words: packed maxima of magnitudes
+// (max.xorsign.abs keeps |.| in bits 14:0 of each half), then the larger half.
+template <bool BF16>
+__device__ __forceinline__ float block_amax(const U32x8& in) {
+  uint32_t m[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (BF16)
+      asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m[k]) : "r"(in.w[2 * k]), "r"(in.w[2 * k + 1]));
+    else
+      asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(m[k]) : "r"(in.w[2 * k]), "r"(in.w[2 * k + 1]));
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    if (BF16)
+      asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m[k]) : "r"(m[k]), "r"(m[k + 2]));
+    else
+      asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(m[k]) : "r"(m[k]), "r"(m[k + 2]));
+  }
+  uint32_t t;
+  if (BF16)
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(t) : "r"(m[0]), "r"(m[1]));
+  else
+    asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(t) : "r"(m[0]), "r"(m[1]));
+  const uint32_t mag = max(t & 0x7FFFu, (t >> 16) & 0x7FFFu);  // magnitudes order like ints
+  return BF16 ? __uint_as_float(mag << 16)
+              : __half2float(__ushort_as_half(static_cast<unsigned short>(mag)));
 }
 
 // Four element pairs (x[0..7]) with multiplier inv: the four code bytes, and the decoded
@@ -181,7 +211,11 @@ __device__ __forceinline__ float candidate_f16(const float x[16], const uint32_t
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const uint32_t e = hfma2_rn(t[k], neg_sg2, xh[k]);
-    t[k] = MSE ? hsq2_rn(e, nzh2) : (e & 0x7FFF7FFFu);
+    if (MSE) {
+      t[k] = hsq2_rn(e, nzh2);
+    } else {
+      asm("abs.f16x2 %0, %1;" : "=r"(t[k]) : "r"(e));
+    }
   }
 #pragma unroll
   for (int k = 0; k < 4; ++k) t[k] = hadd2_rn(t[k], t[k + 4]);
@@ -209,9 +243,7 @@ __device__ __forceinline__ BlockOut quantize_block(const U32x8& in, const Tensor
                                                    uint32_t nz) {
   float x[16];
   unpack16<BF16>(in, x);
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  const float amax = block_amax<BF16>(in);
   const float ra = fminf(quotient(amax, tc.g6, tc.r6, tc.exact_rcp), cap_a);
   BlockOut r;
   if (MODE == 0) {
@@ -245,24 +277,66 @@ __device__ __forceinline__ BlockOut quantize_block(const U32x8& in, const Tensor
   return r;
 }
 
-template <bool BF16, int MODE, bool VEC256>
-__global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
-  __shared__ Tables tab;
+// Fill the per-CTA tables for both tensors' global scales; ends with __syncthreads().
+__device__ __forceinline__ void fill_tables(Tables& tab, const float gs[2]) {
   for (int s = threadIdx.x; s < 256; s += blockDim.x) {
     const uint32_t S2 = f16x2_from_e4m3x2(static_cast<uint32_t>(s) * 0x0101u);
     const float S = f32_from_f16_lo(S2);
     tab.S2[s] = S2;
 #pragma unroll
     for (int kv = 0; kv < 2; ++kv) {
-      const float den = __fmul_rn(S, a.gs[kv]);
+      const float den = __fmul_rn(S, gs[kv]);
       tab.inv[kv][s] = den == 0.0f ? 0.0f : fminf(__frcp_rn(den), FLT_MAX);
-      const __half gh = __float2half_rn(a.gs[kv]);
+      const __half gh = __float2half_rn(gs[kv]);
       const __half sg = __hmul_rn(__ushort_as_half(static_cast<unsigned short>(S2 & 0xFFFFu)), gh);
       const uint32_t n = static_cast<uint32_t>(__half_as_ushort(sg)) ^ 0x8000u;
       tab.neg_sg2[kv][s] = n | (n << 16);
     }
   }
   __syncthreads();
+}
+
+// Destination of appended row i: request batch_indices[i], logical position positions[i],
+// page kv_indices[kv_indptr[b] + pos / page_size], slot pos % page_size. Rows outside the
+// described space or with a page outside a pool are reported and marked invalid.
+struct RowMeta {
+  int32_t page;   // physical page (valid only with flags bit 0 / bit 1)
+  int32_t slot;   // slot inside the page
+  int32_t flags;  // bit 0: K page valid, bit 1: V page valid
+  int32_t pad;
+};
+
+__device__ __forceinline__ RowMeta resolve_row(const AppendArgs& a, int64_t i) {
+  RowMeta m{0, 0, 0, 0};
+  const int32_t b = __ldg(a.batch_indices + i);
+  const int32_t pos = __ldg(a.positions + i);
+  if (b < 0 || b >= a.batch_size) {
+    flag(a.status, NVFP4_DEV_BAD_BATCH);
+    return m;
+  }
+  const int64_t start = __ldg(a.kv_indptr + b);
+  const int64_t npages = static_cast<int64_t>(__ldg(a.kv_indptr + b + 1)) - start;
+  const int64_t lp = pos >= 0 ? div_q(pos, a.div_ps) : -1;
+  bool ok = pos >= 0 && lp < npages && start >= 0 && start + lp < a.num_kv_indices;
+  if (ok && a.kv_last_page_len) ok = pos < (npages - 1) * a.ps + __ldg(a.kv_last_page_len + b);
+  if (!ok) {
+    flag(a.status, NVFP4_DEV_BAD_POSITION);
+    return m;
+  }
+  const int64_t page = __ldg(a.kv_indices + start + lp);
+  m.page = static_cast<int32_t>(page);
+  m.slot = static_cast<int32_t>(pos - lp * a.ps);
+  const bool kok = page >= 0 && page < a.kc.num_pages;
+  const bool vok = page >= 0 && page < a.vc.num_pages;
+  if (!kok || !vok) flag(a.status, NVFP4_DEV_BAD_PAGE);
+  m.flags = (kok ? 1 : 0) | (vok ? 2 : 0);
+  return m;
+}
+
+template <bool BF16, int MODE, bool VEC256>
+__global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
+  __shared__ Tables tab;
+  fill_tables(tab, a.gs);
   const TensorConsts tck = make_consts(a.gs[0]);
   const TensorConsts tcv = make_consts(a.gs[1]);
 
@@ -316,6 +390,190 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   }
 }
 
+// ---- TMA-fed variant ------------------------------------------------------------------
+//
+// A tile is `rows` consecutive appended tokens, all heads, of K and of V. The producer warp
+// resolves the destination page of each row (one lane per row, so the dependent index
+// loads overlap), writes it into the stage, and bulk-copies the tile's K and V rows into
+// shared memory. The consumer warps quantize blocks straight from shared memory: thread k
+// of a tile takes block k of K and block k of V (a row's blocks are contiguous there).
+
+// Destination of one appended row in both caches, resolved once per row by the producer:
+// the addresses of (page, slot, head 0, block 0) in the K and V codes and scales; null when
+// the row or its page is invalid. Head h, block j of the row is at
+// base + h * head_step + {8 j | j}.
+struct RowDst {
+  uint8_t* kd;
+  uint8_t* ks;
+  uint8_t* vd;
+  uint8_t* vs;
+};
+
+__device__ __forceinline__ RowDst resolve_row_dst(const AppendArgs& a, int64_t i) {
+  RowDst d{nullptr, nullptr, nullptr, nullptr};
+  const RowMeta m = resolve_row(a, i);
+  const int64_t rd = a.layout == NVFP4_NHD ? static_cast<int64_t>(a.H) * (a.D / 2) : a.D / 2;
+  const int64_t rs = a.layout == NVFP4_NHD ? static_cast<int64_t>(a.H) * a.nb : a.nb;
+  if (m.flags & 1) {
+    d.kd = a.kc.data + m.page * a.kc.data_page_stride + m.slot * rd;
+    d.ks = a.kc.sf + m.page * a.kc.sf_page_stride + m.slot * rs;
+  }
+  if (m.flags & 2) {
+    d.vd = a.vc.data + m.page * a.vc.data_page_stride + m.slot * rd;
+    d.vs = a.vc.sf + m.page * a.vc.sf_page_stride + m.slot * rs;
+  }
+  return d;
+}
+
+struct AppendTmaLayout {
+  uint32_t rows;        // tokens per tile
+  uint32_t row_bytes;   // H * D * 2 (one row of one tensor)
+  uint32_t stage_bytes; // K tile + V tile + row destinations
+  uint32_t tables_off, stages_off, bars_off, misc_off, total;
+  int ns;
+};
+
+inline AppendTmaLayout append_tma_layout(uint32_t rows, uint32_t row_bytes, int ns) {
+  AppendTmaLayout L;
+  L.rows = rows;
+  L.row_bytes = row_bytes;
+  L.stage_bytes = round_up(2u * rows * row_bytes + rows * sizeof(RowDst), 128);
+  L.ns = ns;
+  L.tables_off = 0;
+  L.stages_off = round_up(sizeof(Tables), 128);
+  L.bars_off = L.stages_off + static_cast<uint32_t>(ns) * L.stage_bytes;
+  L.misc_off = L.bars_off + 2u * static_cast<uint32_t>(ns) * 8u;
+  L.total = L.misc_off + 4u * (1u + static_cast<uint32_t>(ns));
+  return L;
+}
+
+template <bool BF16, int MODE>
+__global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const AppendArgs a,
+                                                                  const AppendTmaLayout L) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  Tables& tab = *reinterpret_cast<Tables*>(smem + L.tables_off);
+  uint8_t* stages = smem + L.stages_off;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars_off);
+  uint64_t* empty = full + L.ns;
+  volatile int32_t* s_abort = reinterpret_cast<int32_t*>(smem + L.misc_off);
+  volatile uint32_t* s_issued = reinterpret_cast<uint32_t*>(smem + L.misc_off + 4);
+  const int ns = L.ns;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ns; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, kConsumerWarps);
+      s_issued[s] = 0;
+    }
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  fill_tables(tab, a.gs);  // ends with __syncthreads()
+
+  const int64_t tiles = (a.nnz + L.rows - 1) / L.rows;
+  const uint32_t tile_bytes = L.rows * L.row_bytes;
+  const bool contiguous = a.k_row_bytes == L.row_bytes && a.v_row_bytes == L.row_bytes;
+  if (warp == kConsumerWarps) {
+    int s = 0;
+    uint32_t phase = 0, round = 0;  // phase = parity of `round`, the stage's fill count
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(empty + s, phase ^ 1u) && !*s_abort;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) {
+        if (lane == 0) {
+          *s_abort = 1;
+          flag(a.status, NVFP4_DEV_TIMEOUT);
+        }
+        break;
+      }
+      uint8_t* st = stages + static_cast<uint32_t>(s) * L.stage_bytes;
+      RowDst* dst = reinterpret_cast<RowDst*>(st + 2u * tile_bytes);
+      const int64_t row0 = tile * L.rows;
+      const uint32_t nrows =
+          static_cast<uint32_t>(min(static_cast<int64_t>(L.rows), a.nnz - row0));
+      for (uint32_t r = lane; r < nrows; r += 32) dst[r] = resolve_row_dst(a, row0 + r);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(full + s, 2u * nrows * L.row_bytes);
+      __syncwarp();
+      if (contiguous) {
+        if (lane == 0) {
+          bulk_g2s(st, a.k + row0 * a.k_row_bytes, nrows * L.row_bytes, full + s);
+          bulk_g2s(st + tile_bytes, a.v + row0 * a.v_row_bytes, nrows * L.row_bytes, full + s);
+        }
+      } else {
+        for (uint32_t r = lane; r < nrows; r += 32) {
+          bulk_g2s(st + r * L.row_bytes, a.k + (row0 + r) * a.k_row_bytes, L.row_bytes, full + s);
+          bulk_g2s(st + tile_bytes + r * L.row_bytes, a.v + (row0 + r) * a.v_row_bytes,
+                   L.row_bytes, full + s);
+        }
+      }
+      if (lane == 0) s_issued[s] = round + 1;
+      __syncwarp();
+      if (++s == ns) {
+        s = 0;
+        phase ^= 1u;
+        ++round;
+      }
+    }
+  } else {
+    const int ct = threadIdx.x;
+    const TensorConsts tck = make_consts(a.gs[0]);
+    const TensorConsts tcv = make_consts(a.gs[1]);
+    const int32_t row_blocks = a.H * a.nb;
+    // step between heads of one row: codes, scales
+    const int32_t hsd = a.layout == NVFP4_NHD ? a.D / 2 : a.ps * (a.D / 2);
+    const int32_t hss = a.layout == NVFP4_NHD ? a.nb : a.ps * a.nb;
+    int s = 0;
+    uint32_t phase = 0;
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+      if (*s_abort || !mbar_wait(full + s, phase)) {
+        if (lane == 0) {
+          *s_abort = 1;
+          flag(a.status, NVFP4_DEV_TIMEOUT);
+        }
+        break;
+      }
+      const uint8_t* st = stages + static_cast<uint32_t>(s) * L.stage_bytes;
+      const RowDst* dst = reinterpret_cast<const RowDst*>(st + 2u * tile_bytes);
+      const int32_t nrows =
+          static_cast<int32_t>(min(static_cast<int64_t>(L.rows), a.nnz - tile * L.rows));
+      const int32_t nblk = nrows * row_blocks;
+      for (int32_t k = ct; k < nblk; k += kConsumers) {
+        const int32_t r = div_q32(k, a.div_row_blocks);
+        const int32_t rem = k - r * row_blocks;
+        const int32_t h = div_q32(rem, a.div_nb);
+        const int32_t j = rem - h * a.nb;
+        const RowDst d = dst[r];
+        const int32_t od = h * hsd + 8 * j;
+        const int32_t os = h * hss + j;
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+          uint8_t* pd = kv ? d.vd : d.kd;
+          if (pd == nullptr) continue;
+          const U32x8 x = ld_shared_256(st + kv * tile_bytes + 32 * k);
+          const BlockOut q =
+              quantize_block<BF16, MODE>(x, kv ? tcv : tck, tab, kv, a.cap_a, a.neg_zero);
+          *reinterpret_cast<uint2*>(pd + od) = make_uint2(q.c0, q.c1);
+          (kv ? d.vs : d.ks)[os] = static_cast<uint8_t>(q.s);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + s);
+      if (++s == ns) {
+        s = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  // no copy may still be landing in this CTA's shared memory when it exits
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ns; ++s)
+      if (s_issued[s] > 0) mbar_wait(full + s, (s_issued[s] - 1) & 1u);
+  }
+}
+
 template <bool BF16, int MODE, bool VEC256>
 nvfp4_status launch_t(const AppendArgs& a, cudaStream_t stream) {
   const auto kern = append_kernel<BF16, MODE, VEC256>;
@@ -329,8 +587,34 @@ nvfp4_status launch_t(const AppendArgs& a, cudaStream_t stream) {
   return check_launch("nvfp4_quantize_append_paged");
 }
 
+// TMA path: tiles of up to 32 rows and about 16 KB per tensor, 2 to 6 stages in 70 KB
+// (three CTAs per SM).
+template <bool BF16, int MODE>
+nvfp4_status launch_tma(const AppendArgs& a, uint32_t row_bytes, cudaStream_t stream) {
+  const auto kern = append_tma_kernel<BF16, MODE>;
+  uint32_t rows = 16384u / row_bytes;
+  rows = rows < 1 ? 1 : (rows > 32 ? 32 : rows);
+  const uint32_t one = round_up(2u * rows * row_bytes + rows * sizeof(RowDst), 128);
+  int ns = static_cast<int>((70u * 1024u) / one);
+  ns = ns < 2 ? 2 : (ns > 6 ? 6 : ns);
+  const AppendTmaLayout L = append_tma_layout(rows, row_bytes, ns);
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       static_cast<int>(L.total));
+  const int64_t tiles = (a.nnz + rows - 1) / rows;
+  const int64_t cap = static_cast<int64_t>(sm_count()) *
+                      blocks_per_sm(reinterpret_cast<const void*>(kern), kTmaThreads, L.total);
+  const int grid = static_cast<int>(tiles < cap ? tiles : cap);
+  if (grid <= 0) return NVFP4_OK;
+  kern<<<grid, kTmaThreads, L.total, stream>>>(a, L);
+  return check_launch("nvfp4_quantize_append_paged");
+}
+
 template <bool BF16, int MODE>
 nvfp4_status launch_v(const AppendArgs& a, bool vec256, cudaStream_t s) {
+  // one row of K and V (all heads) must fit a stage; bases and row strides are 16-byte
+  // aligned by the entry point's checks
+  const int64_t row_bytes = static_cast<int64_t>(a.H) * a.D * 2;
+  if (2 * row_bytes <= 48 * 1024) return launch_tma<BF16, MODE>(a, static_cast<uint32_t>(row_bytes), s);
   return vec256 ? launch_t<BF16, MODE, true>(a, s) : launch_t<BF16, MODE, false>(a, s);
 }
 

@@ -13,6 +13,7 @@
 // store covers 1 KB of contiguous output; up to eight blocks per thread are loaded before any
 // is decoded to keep enough bytes in flight.
 #include "internal.h"
+#include "pipeline.cuh"
 #include "scan.cuh"
 
 namespace nvfp4 {
@@ -120,6 +121,152 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const DequantArgs a) 
   }
 }
 
+// ---- TMA-fed variant ------------------------------------------------------------------
+//
+// Warp kConsumerWarps (the producer) walks the item list: it resolves the page index and
+// bulk-copies the page's codes and scales into the next free stage of a shared-memory
+// ring, with the item's geometry alongside. The consumer warps decode from shared memory
+// and stream the 32-byte output stores, so no warp waits on HBM latency while it could be
+// decoding.
+
+template <bool OUT_BF16, bool BT64>
+__global__ void __launch_bounds__(kTmaThreads, 2) dequant_tma_kernel(const DequantArgs a,
+                                                                  const TmaLayout L) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  int32_t* s_cum = reinterpret_cast<int32_t*>(smem);
+  uint8_t* stages = smem + L.stages_off;
+  StageMeta* meta = reinterpret_cast<StageMeta*>(smem + L.meta_off);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars_off);
+  uint64_t* empty = full + L.ns;
+  volatile int32_t* s_abort = reinterpret_cast<int32_t*>(smem + L.misc_off);
+  volatile uint32_t* s_issued = reinterpret_cast<uint32_t*>(smem + L.misc_off + 4);
+  const int ns = L.ns;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ns; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, kConsumerWarps);
+      s_issued[s] = 0;
+    }
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  const int32_t L_out = a.L;
+  const int32_t ps = a.ps;
+  const int32_t cap = static_cast<int32_t>(min(static_cast<int64_t>(L_out), a.max_pages * ps));
+  block_inclusive_scan(s_cum, a.B, [&](int32_t b) {  // ends with __syncthreads()
+    int32_t len = __ldg(a.seq_lens + b);
+    if (len > cap) {
+      flag(a.status, NVFP4_DEV_LEN_CLAMPED);
+      len = cap;
+    }
+    return len > 0 ? (len + ps - 1) / ps : 0;
+  });
+  const int64_t items = 2 * static_cast<int64_t>(s_cum[a.B - 1]);
+
+  if (warp == kConsumerWarps) {
+    // producer: lane 0 issues, the warp stays converged
+    int s = 0;
+    uint32_t round = 0;  // how many times stage s has been used before
+    for (int64_t item = blockIdx.x; item < items;
+         item += gridDim.x, s = (s + 1 == ns) ? 0 : s + 1, round += (s == 0)) {
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(empty + s, (round & 1u) ^ 1u) && !*s_abort;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) {
+        if (lane == 0) {
+          *s_abort = 1;
+          flag(a.status, NVFP4_DEV_TIMEOUT);
+        }
+        break;
+      }
+      if (lane == 0) {
+        const int kv = static_cast<int>(item & 1);
+        const int32_t pi = static_cast<int32_t>(item >> 1);
+        const int32_t b = scan_find(s_cum, a.B, pi);
+        const int32_t j = pi - (b > 0 ? s_cum[b - 1] : 0);
+        const int32_t len = min(__ldg(a.seq_lens + b), cap);
+        const int32_t t0 = j * ps;
+        const int64_t tcol = static_cast<int64_t>(b) * a.max_pages + j;
+        const int64_t page =
+            BT64 ? __ldg(reinterpret_cast<const int64_t*>(a.block_tables) + tcol)
+                 : __ldg(reinterpret_cast<const int32_t*>(a.block_tables) + tcol);
+        const uint8_t* data = kv ? a.vc.data : a.kc.data;
+        const uint8_t* sf = kv ? a.vc.sf : a.kc.sf;
+        const int64_t dps = kv ? a.vc.data_page_stride : a.kc.data_page_stride;
+        const int64_t sps = kv ? a.vc.sf_page_stride : a.kc.sf_page_stride;
+        const bool valid = page >= 0 && page < (kv ? a.vc.num_pages : a.kc.num_pages);
+        StageMeta m;
+        m.f0 = b;
+        m.f1 = t0;
+        m.f2 = min(ps, len - t0);
+        m.flags = kv | (valid ? 2 : 0);
+        meta[s] = m;
+        uint8_t* st = stages + static_cast<uint32_t>(s) * L.stage_bytes;
+        if (valid) {
+          mbar_arrive_expect_tx(full + s, L.codes_bytes + L.sf_bytes);
+          bulk_g2s(st, data + page * dps, L.codes_bytes, full + s);
+          bulk_g2s(st + L.sf_off, sf + page * sps, L.sf_bytes, full + s);
+        } else {
+          flag(a.status, NVFP4_DEV_BAD_PAGE);
+          mbar_arrive(full + s);
+        }
+        s_issued[s] = round + 1;
+      }
+      __syncwarp();
+    }
+  } else {
+    const int ct = threadIdx.x;  // 0 .. kConsumers-1
+    const int32_t row_blocks = a.H * a.nb;
+    const int64_t row_bytes = static_cast<int64_t>(a.H) * a.D * 2;
+    const float gs_k = __ldg(a.k_scale);
+    const float gs_v = __ldg(a.v_scale);
+    int s = 0;
+    uint32_t round = 0;  // how many times stage s has been used before
+    for (int64_t item = blockIdx.x; item < items;
+         item += gridDim.x, s = (s + 1 == ns) ? 0 : s + 1, round += (s == 0)) {
+      if (*s_abort || !mbar_wait(full + s, round & 1u)) {
+        if (lane == 0) {
+          *s_abort = 1;
+          flag(a.status, NVFP4_DEV_TIMEOUT);
+        }
+        break;
+      }
+      const StageMeta m = meta[s];
+      if (m.flags & 2) {
+        const uint8_t* st = stages + static_cast<uint32_t>(s) * L.stage_bytes;
+        const uint8_t* sfp = st + L.sf_off;
+        uint8_t* ob = ((m.flags & 1) ? a.out_v : a.out_k) +
+                      (static_cast<int64_t>(m.f0) * L_out + m.f1) * row_bytes;
+        const float gs = (m.flags & 1) ? gs_v : gs_k;
+        const int32_t nblk = m.f2 * row_blocks;
+#pragma unroll 4
+        for (int32_t k = ct; k < nblk; k += kConsumers) {
+          int32_t off = k;  // NHD: block index inside the page equals k
+          if (a.layout == NVFP4_HND) {
+            const int32_t slot = static_cast<int32_t>(div_q(k, a.div_row_blocks));
+            const int32_t rem = k - slot * row_blocks;
+            const int32_t h = static_cast<int32_t>(div_q(rem, a.div_nb));
+            off = (h * ps + slot) * a.nb + (rem - h * a.nb);
+          }
+          const uint2 codes = *reinterpret_cast<const uint2*>(st + 8 * off);
+          const U32x8 o = decode_block<OUT_BF16>(codes, sfp[off], gs);
+          st_256(ob + static_cast<int64_t>(k) * 32, o);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + s);
+    }
+  }
+  // no copy may still be landing in this CTA's shared memory when it exits
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ns; ++s)
+      if (s_issued[s] > 0) mbar_wait(full + s, (s_issued[s] - 1) & 1u);
+  }
+}
+
 template <bool OUT_BF16, bool BT64, bool VEC256>
 nvfp4_status launch_t(const DequantArgs& a, cudaStream_t stream) {
   const auto kern = dequant_kernel<OUT_BF16, BT64, VEC256>;
@@ -133,8 +280,32 @@ nvfp4_status launch_t(const DequantArgs& a, cudaStream_t stream) {
   return check_launch("nvfp4_dequantize_paged");
 }
 
+// The TMA path needs bulk-copyable pages and a 32-byte aligned output.
+bool tma_eligible(const DequantArgs& a, bool vec256, uint32_t& codes_bytes, uint32_t& sf_bytes) {
+  const int64_t cb = static_cast<int64_t>(a.ps) * a.H * (a.D / 2);
+  const int64_t sb = static_cast<int64_t>(a.ps) * a.H * (a.D / 16);
+  codes_bytes = static_cast<uint32_t>(cb);
+  sf_bytes = static_cast<uint32_t>(sb);
+  return vec256 && pages_bulk_copyable(a.kc, a.vc, cb, sb);
+}
+
+template <bool OUT_BF16, bool BT64>
+nvfp4_status launch_tma(const DequantArgs& a, uint32_t codes_bytes, uint32_t sf_bytes,
+                        cudaStream_t stream) {
+  const auto kern = dequant_tma_kernel<OUT_BF16, BT64>;
+  const TmaLayout L = tma_layout(a.B, codes_bytes, sf_bytes, stages_for(codes_bytes, sf_bytes));
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       static_cast<int>(L.total));
+  const int grid =
+      sm_count() * blocks_per_sm(reinterpret_cast<const void*>(kern), kTmaThreads, L.total);
+  kern<<<grid, kTmaThreads, L.total, stream>>>(a, L);
+  return check_launch("nvfp4_dequantize_paged");
+}
+
 template <bool OUT_BF16, bool BT64>
 nvfp4_status launch_v(const DequantArgs& a, bool vec256, cudaStream_t s) {
+  uint32_t cb, sb;
+  if (tma_eligible(a, vec256, cb, sb)) return launch_tma<OUT_BF16, BT64>(a, cb, sb, s);
   return vec256 ? launch_t<OUT_BF16, BT64, true>(a, s) : launch_t<OUT_BF16, BT64, false>(a, s);
 }
 

@@ -193,6 +193,16 @@ __device__ __forceinline__ U32x8 ld_nc_2x128(const void* p) {
   return r;
 }
 
+// 32 bytes from shared memory (address 16-byte aligned).
+__device__ __forceinline__ U32x8 ld_shared_256(const void* p) {
+  U32x8 r;
+  const uint4 a = reinterpret_cast<const uint4*>(p)[0];
+  const uint4 b = reinterpret_cast<const uint4*>(p)[1];
+  r.w[0] = a.x; r.w[1] = a.y; r.w[2] = a.z; r.w[3] = a.w;
+  r.w[4] = b.x; r.w[5] = b.y; r.w[6] = b.z; r.w[7] = b.w;
+  return r;
+}
+
 // 32-byte store (address 32-byte aligned).
 __device__ __forceinline__ void st_256(void* p, const U32x8& v) {
   asm volatile(
@@ -224,6 +234,10 @@ __host__ __device__ inline Div make_div(int64_t d) {
 }
 __device__ __forceinline__ int64_t div_q(int64_t n, Div d) {
   return d.shift >= 0 ? (n >> d.shift) : n / d.d;
+}
+// The same for non-negative 32-bit n with a divisor below 2^31.
+__device__ __forceinline__ int32_t div_q32(int32_t n, Div d) {
+  return d.shift >= 0 ? (n >> d.shift) : n / static_cast<int32_t>(d.d);
 }
 
 }  // namespace nvfp4

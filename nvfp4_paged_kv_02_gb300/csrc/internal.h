@@ -37,7 +37,7 @@ struct AppendArgs {
   int64_t v_row_bytes;
   int64_t nnz;
   int32_t H, D, nb;
-  Div div_nb, div_H, div_ps;
+  Div div_nb, div_H, div_ps, div_row_blocks;
   const int32_t* batch_indices;
   const int32_t* positions;
   nvfp4_paged_cache kc, vc;

@@ -13,6 +13,7 @@
 // 32-byte store out). With HND input, chunk k is also the k-th 16-byte chunk of the input
 // page, so both streams are contiguous.
 #include "internal.h"
+#include "pipeline.cuh"
 #include "scan.cuh"
 
 namespace nvfp4 {
@@ -135,9 +136,178 @@ __global__ void __launch_bounds__(kThreads) materialize_kernel(const Materialize
   }
 }
 
+// ---- TMA-fed variant ------------------------------------------------------------------
+//
+// The producer warp resolves each (active page, K|V) item -- source page, output page --
+// and bulk-copies the source page's codes and scales into the next free shared-memory
+// stage; the consumer warps convert from shared memory and stream the 32-byte stores.
+
+__global__ void __launch_bounds__(kTmaThreads, 2) materialize_tma_kernel(const MaterializeArgs a,
+                                                                       const TmaLayout L) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  int32_t* s_cum = reinterpret_cast<int32_t*>(smem);
+  uint8_t* stages = smem + L.stages_off;
+  StageMeta* meta = reinterpret_cast<StageMeta*>(smem + L.meta_off);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars_off);
+  uint64_t* empty = full + L.ns;
+  volatile int32_t* s_abort = reinterpret_cast<int32_t*>(smem + L.misc_off);
+  volatile uint32_t* s_issued = reinterpret_cast<uint32_t*>(smem + L.misc_off + 4);
+  const int ns = L.ns;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ns; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, kConsumerWarps);
+      s_issued[s] = 0;
+    }
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  const int32_t ps = a.ps;
+  const int32_t mpps = a.mpps;
+  block_inclusive_scan(s_cum, a.B, [&](int32_t b) {  // ends with __syncthreads()
+    const int32_t len = __ldg(a.seq_lens + b);
+    int32_t n = len > 0 ? static_cast<int32_t>((static_cast<int64_t>(len) + ps - 1) / ps) : 0;
+    if (n > mpps) {
+      flag(a.status, NVFP4_DEV_LEN_CLAMPED);
+      n = mpps;
+    }
+    return n;
+  });
+  const int64_t half_page = static_cast<int64_t>(a.H) * ps * a.D;
+  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t gstep = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t q = gtid; q < 2 * half_page / 16; q += gstep)
+    reinterpret_cast<uint4*>(a.out)[q] = make_uint4(0, 0, 0, 0);
+  const int64_t entries = static_cast<int64_t>(a.B) * mpps;
+  for (int64_t e = gtid; e < entries; e += gstep) {
+    const int32_t b = static_cast<int32_t>(div_q(e, a.div_mpps));
+    const int32_t j = static_cast<int32_t>(e - static_cast<int64_t>(b) * mpps);
+    const int32_t n = s_cum[b] - (b > 0 ? s_cum[b - 1] : 0);
+    if (j < n) {
+      const int64_t base = a.kv_page_indptr ? __ldg(a.kv_page_indptr + b)
+                                            : static_cast<int64_t>(b) * mpps;
+      a.tables[e] = static_cast<int32_t>(base + j + 1);
+    } else if (a.zero_tables) {
+      a.tables[e] = 0;
+    }
+  }
+  const int64_t items = 2 * static_cast<int64_t>(s_cum[a.B - 1]);
+
+  if (warp == kConsumerWarps) {
+    int s = 0;
+    uint32_t round = 0;  // how many times stage s has been used before
+    for (int64_t item = blockIdx.x; item < items;
+         item += gridDim.x, s = (s + 1 == ns) ? 0 : s + 1, round += (s == 0)) {
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(empty + s, (round & 1u) ^ 1u) && !*s_abort;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) {
+        if (lane == 0) {
+          *s_abort = 1;
+          flag(a.status, NVFP4_DEV_TIMEOUT);
+        }
+        break;
+      }
+      if (lane == 0) {
+        const int kv = static_cast<int>(item & 1);
+        const int32_t pi = static_cast<int32_t>(item >> 1);
+        const int32_t b = scan_find(s_cum, a.B, pi);
+        const int32_t j = pi - (b > 0 ? s_cum[b - 1] : 0);
+        const int64_t tcol = a.shared ? static_cast<int64_t>(b) * a.max_num_pages + j
+                                      : (static_cast<int64_t>(b) * 2 + kv) * a.max_num_pages + j;
+        const int64_t page = __ldg(a.block_tables + tcol);
+        const int64_t base = a.kv_page_indptr ? __ldg(a.kv_page_indptr + b)
+                                              : static_cast<int64_t>(b) * mpps;
+        const int64_t o = base + j + 1;
+        const bool page_ok = page >= 0 && page < (kv ? a.vc.num_pages : a.kc.num_pages);
+        const bool out_ok = o >= 1 && o < a.out_num_pages;
+        if (!page_ok) flag(a.status, NVFP4_DEV_BAD_PAGE);
+        else if (!out_ok) flag(a.status, NVFP4_DEV_BAD_OUT_PAGE);
+        const bool valid = page_ok && out_ok;
+        StageMeta m;
+        m.f0 = static_cast<int32_t>(valid ? o : 0);
+        m.f1 = kv;
+        m.f2 = 0;
+        m.flags = valid ? 2 : 0;
+        meta[s] = m;
+        uint8_t* st = stages + static_cast<uint32_t>(s) * L.stage_bytes;
+        if (valid) {
+          const uint8_t* data = kv ? a.vc.data : a.kc.data;
+          const uint8_t* sf = kv ? a.vc.sf : a.kc.sf;
+          const int64_t dps = kv ? a.vc.data_page_stride : a.kc.data_page_stride;
+          const int64_t sps = kv ? a.vc.sf_page_stride : a.kc.sf_page_stride;
+          mbar_arrive_expect_tx(full + s, L.codes_bytes + L.sf_bytes);
+          bulk_g2s(st, data + page * dps, L.codes_bytes, full + s);
+          bulk_g2s(st + L.sf_off, sf + page * sps, L.sf_bytes, full + s);
+        } else {
+          mbar_arrive(full + s);
+        }
+        s_issued[s] = round + 1;
+      }
+      __syncwarp();
+    }
+  } else {
+    const int ct = threadIdx.x;
+    const int32_t row_chunks = a.D / 32;
+    const int32_t chunks = a.H * ps * row_chunks;
+    int s = 0;
+    uint32_t round = 0;  // how many times stage s has been used before
+    for (int64_t item = blockIdx.x; item < items;
+         item += gridDim.x, s = (s + 1 == ns) ? 0 : s + 1, round += (s == 0)) {
+      if (*s_abort || !mbar_wait(full + s, round & 1u)) {
+        if (lane == 0) {
+          *s_abort = 1;
+          flag(a.status, NVFP4_DEV_TIMEOUT);
+        }
+        break;
+      }
+      const StageMeta m = meta[s];
+      if (m.flags & 2) {
+        const uint8_t* st = stages + static_cast<uint32_t>(s) * L.stage_bytes;
+        const uint8_t* sfp = st + L.sf_off;
+        uint8_t* dst = a.out + (static_cast<int64_t>(m.f0) * 2 + m.f1) * half_page;
+#pragma unroll 4
+        for (int32_t k = ct; k < chunks; k += kConsumers) {
+          int32_t off = k;  // HND: chunk k of the output is chunk k of the input page
+          if (a.layout == NVFP4_NHD) {
+            const int32_t h = static_cast<int32_t>(div_q(k, a.div_page_chunks));
+            const int32_t rem = k - h * (ps * row_chunks);
+            const int32_t slot = static_cast<int32_t>(div_q(rem, a.div_row_chunks));
+            off = (slot * a.H + h) * row_chunks + (rem - slot * row_chunks);
+          }
+          const uint4 c = *reinterpret_cast<const uint4*>(st + 16 * off);
+          const uint32_t s01 = *reinterpret_cast<const uint16_t*>(sfp + 2 * off);
+          st_256(dst + static_cast<int64_t>(k) * 32, convert_chunk(c, s01));
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + s);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ns; ++s)
+      if (s_issued[s] > 0) mbar_wait(full + s, (s_issued[s] - 1) & 1u);
+  }
+}
+
 }  // namespace
 
 nvfp4_status launch_materialize(const MaterializeArgs& a, cudaStream_t stream) {
+  const int64_t cb = static_cast<int64_t>(a.ps) * a.H * (a.D / 2);
+  const int64_t sb = static_cast<int64_t>(a.ps) * a.H * (a.D / 16);
+  if (pages_bulk_copyable(a.kc, a.vc, cb, sb)) {
+    const auto kern = materialize_tma_kernel;
+    const TmaLayout L = tma_layout(a.B, static_cast<uint32_t>(cb), static_cast<uint32_t>(sb),
+                                   stages_for(static_cast<uint32_t>(cb), static_cast<uint32_t>(sb)));
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(L.total));
+    const int grid =
+        sm_count() * blocks_per_sm(reinterpret_cast<const void*>(kern), kTmaThreads, L.total);
+    kern<<<grid, kTmaThreads, L.total, stream>>>(a, L);
+    return check_launch("nvfp4_materialize_fp8");
+  }
   const auto kern = materialize_kernel;
   const size_t smem = static_cast<size_t>(a.B) * sizeof(int32_t);
   if (smem > 48 * 1024) {

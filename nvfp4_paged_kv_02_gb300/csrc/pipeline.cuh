@@ -1,0 +1,130 @@
+// pipeline.cuh -- shared-memory stage ring fed by TMA bulk copies (sm_90+ forms, used on
+// sm_103a): mbarrier init / arrive / transaction counts / bounded waits and the
+// global -> shared cp.async.bulk.
+//
+// Every wait is bounded: mbar_wait() gives up after kWaitLimit polls and returns false, so
+// a kernel can record an error, stop issuing copies, wait (again bounded) for its own
+// copies in flight and return, instead of spinning forever.
+#pragma once
+
+#include <cstdint>
+
+#include "../../include/nvfp4kv.h"
+
+namespace nvfp4 {
+
+// Polls of mbarrier.try_wait before a wait is abandoned (each poll may itself suspend the
+// thread for a short, hardware-defined time).
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+// Make initialized barriers visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Arrive and announce `bytes` of TMA traffic that will complete on this barrier.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of parity `parity` to complete; false after kWaitLimit polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from global to
+// this CTA's shared memory, completing as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// ---- page-stage ring layout shared by the TMA-fed paged kernels ------------------------
+//
+// Dynamic shared memory: [per-request scan: B int32][ns stages: codes | scales]
+// [ns StageMeta][ns full + ns empty mbarriers][abort flag][ns issue counters].
+// Warp kConsumerWarps produces (bulk copies), warps 0..kConsumerWarps-1 consume.
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kTmaThreads = kConsumers + 32;
+
+struct StageMeta {
+  int32_t f0, f1, f2, flags;  // item fields chosen by the kernel; flags bit 1 = page valid
+};
+
+struct TmaLayout {
+  uint32_t codes_bytes, sf_bytes;  // one page of one tensor
+  uint32_t sf_off, stage_bytes;    // inside a stage
+  uint32_t stages_off, meta_off, bars_off, misc_off, total;
+  int ns;
+};
+
+__host__ __device__ inline uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline TmaLayout tma_layout(int B, uint32_t codes_bytes, uint32_t sf_bytes,
+                                                int ns) {
+  TmaLayout L;
+  L.codes_bytes = codes_bytes;
+  L.sf_bytes = sf_bytes;
+  L.sf_off = round_up(codes_bytes, 128);
+  L.stage_bytes = L.sf_off + round_up(sf_bytes, 128);
+  L.ns = ns;
+  L.stages_off = round_up(static_cast<uint32_t>(B) * 4u, 128);
+  L.meta_off = L.stages_off + static_cast<uint32_t>(ns) * L.stage_bytes;
+  L.bars_off = L.meta_off + static_cast<uint32_t>(ns) * sizeof(StageMeta);
+  L.misc_off = L.bars_off + 2u * static_cast<uint32_t>(ns) * 8u;
+  L.total = L.misc_off + 4u * (1u + static_cast<uint32_t>(ns));
+  return L;
+}
+
+// Stages that fit in `budget` bytes, between 2 and 8.
+inline int stages_for(uint32_t codes_bytes, uint32_t sf_bytes, uint32_t budget = 96u * 1024u) {
+  const uint32_t one = round_up(codes_bytes, 128) + round_up(sf_bytes, 128);
+  int ns = static_cast<int>(budget / one);
+  return ns < 2 ? 2 : (ns > 8 ? 8 : ns);
+}
+
+// Whether one page of each cache can be bulk-copied: 16-byte aligned bases and strides,
+// copy sizes a multiple of 16, and a stage small enough for two per CTA.
+inline bool pages_bulk_copyable(const nvfp4_paged_cache& k, const nvfp4_paged_cache& v,
+                                int64_t codes_bytes, int64_t sf_bytes) {
+  auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  return codes_bytes % 16 == 0 && sf_bytes % 16 == 0 && codes_bytes + sf_bytes <= 48 * 1024 &&
+         al(k.data) && al(k.sf) && al(v.data) && al(v.sf) && k.data_page_stride % 16 == 0 &&
+         v.data_page_stride % 16 == 0 && k.sf_page_stride % 16 == 0 && v.sf_page_stride % 16 == 0;
+}
+
+}  // namespace nvfp4
