@@ -186,12 +186,11 @@ class Step:
         nv.nvfp4_make_global_scale(self.k, self.recipe, out=self.gk)
         nv.nvfp4_make_global_scale(self.v, self.recipe, out=self.gv)
         rec(1)
-        # the append API takes the scales as host floats
-        gs_k, gs_v = float(self.gk.item()), float(self.gv.item())
         rec(2)
+        # the scales stay on the device: no host round trip inside the step
         nv.nvfp4_quantize_append_paged(self.k, self.v, self.bi, self.pos, self.cache, self.sf,
-                                       self.kv_indices, self.kv_indptr, self.last, gs_k, gs_v,
-                                       self.lay, self.recipe, self.status)
+                                       self.kv_indices, self.kv_indptr, self.last, self.gk,
+                                       self.gv, self.lay, self.recipe, self.status)
         rec(3)
         nv.nvfp4_dequantize_paged(self.cache, self.sf, self.bt, self.seq_lens, self.gk, self.gv,
                                   self.out_k, self.out_v, self.lay, self.status)

@@ -80,6 +80,7 @@ typedef int32_t nvfp4_status;
 #define NVFP4_DEV_LEN_CLAMPED 8   /* a sequence length beyond the output extent, clamped */
 #define NVFP4_DEV_BAD_OUT_PAGE 16 /* materialize: output page index outside the workspace */
 #define NVFP4_DEV_TIMEOUT 32      /* a pipeline wait gave up (the kernel stopped early) */
+#define NVFP4_DEV_BAD_SCALE 64    /* a device-held global scale is not positive finite */
 
 /* A 4over6 recipe ("NVFP44Over6Config"; "NVFP4 4over6 Recipes" section). A NULL recipe
  * pointer means standard NVFP4 (4over6 off), as None does in the pages' kernel drivers.
@@ -169,6 +170,21 @@ nvfp4_status nvfp4_quantize_append_paged(
     const int32_t* kv_indices, int64_t num_kv_indices, const int32_t* kv_indptr,
     const int32_t* kv_last_page_len, int32_t batch_size, float k_scale, float v_scale,
     const nvfp4_4over6_config* recipe, int32_t* dev_status, void* stream);
+
+/* nvfp4_quantize_append_paged with the two global decode scales read from device memory
+ * (k_scale, v_scale: one float each, for example the outputs of nvfp4_make_global_scale),
+ * so a step needs no host round trip between computing the scales and using them. Same
+ * arguments and behaviour otherwise. A scale that is not positive finite is reported as
+ * NVFP4_DEV_BAD_SCALE and nothing is written. */
+nvfp4_status nvfp4_quantize_append_paged_dev_scale(
+    const void* append_key, const void* append_value, int32_t dtype, int64_t nnz,
+    int32_t num_kv_heads, int32_t head_dim, int64_t key_row_stride, int64_t value_row_stride,
+    const int32_t* batch_indices, const int32_t* positions, nvfp4_paged_cache k_cache,
+    nvfp4_paged_cache v_cache, int32_t page_size, int32_t kv_layout,
+    const int32_t* kv_indices, int64_t num_kv_indices, const int32_t* kv_indptr,
+    const int32_t* kv_last_page_len, int32_t batch_size, const float* k_scale,
+    const float* v_scale, const nvfp4_4over6_config* recipe, int32_t* dev_status,
+    void* stream);
 
 /* Dequantize a paged NVFP4 cache into contiguous outputs
  * ("flashinfer.quantization.nvfp4_kv_dequantize_paged").

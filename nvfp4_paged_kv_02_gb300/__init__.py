@@ -40,7 +40,7 @@ F16, BF16 = 0, 1
 NHD, HND = 0, 1
 I32, I64 = 0, 1
 DEV_BAD_BATCH, DEV_BAD_POSITION, DEV_BAD_PAGE, DEV_LEN_CLAMPED, DEV_BAD_OUT_PAGE = 1, 2, 4, 8, 16
-DEV_TIMEOUT = 32
+DEV_TIMEOUT, DEV_BAD_SCALE = 32, 64
 
 
 class NVFP4KVError(RuntimeError):
@@ -96,6 +96,10 @@ def load() -> ctypes.CDLL:
         L.nvfp4_quantize_append_paged.argtypes = [
             vp, vp, i32, i64, i32, i32, i64, i64, vp, vp, _Cache, _Cache, i32, i32, vp, i64, vp,
             vp, i32, f32, f32, vp, vp, vp]
+        L.nvfp4_quantize_append_paged_dev_scale.restype = i32
+        L.nvfp4_quantize_append_paged_dev_scale.argtypes = [
+            vp, vp, i32, i64, i32, i32, i64, i64, vp, vp, _Cache, _Cache, i32, i32, vp, i64, vp,
+            vp, i32, vp, vp, vp, vp, vp]
         L.nvfp4_dequantize_paged.restype = i32
         L.nvfp4_dequantize_paged.argtypes = [
             _Cache, _Cache, i32, i32, i32, i32, vp, i32, i32, vp, i32, vp, vp, vp, vp, i32, i32,
@@ -216,10 +220,12 @@ def nvfp4_quantize_append_paged(append_key: torch.Tensor, append_value: torch.Te
                                 batch_indices: torch.Tensor, positions: torch.Tensor,
                                 paged_kv_cache, kv_cache_sf, kv_indices: torch.Tensor,
                                 kv_indptr: torch.Tensor, kv_last_page_len: Optional[torch.Tensor],
-                                k_scale: float, v_scale: float, kv_layout: str = "NHD",
+                                k_scale, v_scale, kv_layout: str = "NHD",
                                 nvfp4_4over6: Optional[NVFP44Over6Config] = None,
                                 dev_status: Optional[torch.Tensor] = None) -> None:
-    """Quantize [nnz, H, D] fp16/bf16 K/V rows and write them into the paged caches."""
+    """Quantize [nnz, H, D] fp16/bf16 K/V rows and write them into the paged caches.
+    k_scale / v_scale: host floats (the pages' form), or 1-element float32 CUDA tensors,
+    which the kernel reads on the device."""
     layout = _layout(kv_layout)
     kc, vc = paged_caches(paged_kv_cache, kv_cache_sf)
     ps, H, D = _dims(kc, layout)
@@ -237,13 +243,22 @@ def nvfp4_quantize_append_paged(append_key: torch.Tensor, append_value: torch.Te
     if kv_last_page_len is not None and kv_last_page_len.dtype != torch.int32:
         raise ValueError("kv_last_page_len must be int32")
     B = kv_indptr.numel() - 1
-    _check("nvfp4_quantize_append_paged", load().nvfp4_quantize_append_paged(
-        _ptr(append_key), _ptr(append_value), _dtype_code(append_key.dtype), nnz, H, D,
-        append_key.stride(0) if nnz else H * D, append_value.stride(0) if nnz else H * D,
-        _ptr(batch_indices), _ptr(positions), kc._c(), vc._c(), ps, layout, _ptr(kv_indices),
-        kv_indices.numel(), _ptr(kv_indptr), _ptr(kv_last_page_len), B, float(k_scale),
-        float(v_scale),
-        _recipe(nvfp4_4over6), _ptr(dev_status), _stream(append_key.device)))
+    common = (_ptr(append_key), _ptr(append_value), _dtype_code(append_key.dtype), nnz, H, D,
+              append_key.stride(0) if nnz else H * D, append_value.stride(0) if nnz else H * D,
+              _ptr(batch_indices), _ptr(positions), kc._c(), vc._c(), ps, layout,
+              _ptr(kv_indices), kv_indices.numel(), _ptr(kv_indptr), _ptr(kv_last_page_len), B)
+    tail = (_recipe(nvfp4_4over6), _ptr(dev_status), _stream(append_key.device))
+    if isinstance(k_scale, torch.Tensor) or isinstance(v_scale, torch.Tensor):
+        # scales held on the device (e.g. from nvfp4_make_global_scale): no host round trip
+        for t in (k_scale, v_scale):
+            if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or t.numel() < 1:
+                raise ValueError("device scales must both be float32 CUDA tensors")
+        _check("nvfp4_quantize_append_paged_dev_scale",
+               load().nvfp4_quantize_append_paged_dev_scale(*common, _ptr(k_scale),
+                                                            _ptr(v_scale), *tail))
+    else:
+        _check("nvfp4_quantize_append_paged", load().nvfp4_quantize_append_paged(
+            *common, float(k_scale), float(v_scale), *tail))
 
 
 def nvfp4_dequantize_paged(paged_kv_cache, kv_cache_sf, block_tables: torch.Tensor,

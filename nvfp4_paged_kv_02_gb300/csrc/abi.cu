@@ -149,24 +149,33 @@ NVFP4_EXPORT nvfp4_status nvfp4_make_global_scale(const void* x, int32_t dtype, 
                              static_cast<cudaStream_t>(stream));
 }
 
-NVFP4_EXPORT nvfp4_status nvfp4_quantize_append_paged(
-    const void* append_key, const void* append_value, int32_t dtype, int64_t nnz,
-    int32_t num_kv_heads, int32_t head_dim, int64_t key_row_stride, int64_t value_row_stride,
-    const int32_t* batch_indices, const int32_t* positions, nvfp4_paged_cache k_cache,
-    nvfp4_paged_cache v_cache, int32_t page_size, int32_t kv_layout,
+}  // extern "C"
+
+namespace {
+
+// Shared body of the two append entry points: scales by value (k_dev == nullptr) or in
+// device memory.
+nvfp4_status append_impl(
+    const char* fn, const void* append_key, const void* append_value, int32_t dtype,
+    int64_t nnz, int32_t num_kv_heads, int32_t head_dim, int64_t key_row_stride,
+    int64_t value_row_stride, const int32_t* batch_indices, const int32_t* positions,
+    nvfp4_paged_cache k_cache, nvfp4_paged_cache v_cache, int32_t page_size, int32_t kv_layout,
     const int32_t* kv_indices, int64_t num_kv_indices, const int32_t* kv_indptr,
     const int32_t* kv_last_page_len, int32_t batch_size, float k_scale, float v_scale,
-    const nvfp4_4over6_config* recipe, int32_t* dev_status, void* stream) {
+    const float* k_dev, const float* v_dev, const nvfp4_4over6_config* recipe,
+    int32_t* dev_status, void* stream) {
   clear_error();
-  const char* fn = "nvfp4_quantize_append_paged";
   if (nvfp4_status st = check_recipe(recipe)) return st;
   if (nvfp4_status st = check_geometry(fn, page_size, num_kv_heads, head_dim, kv_layout)) return st;
   if (dtype != NVFP4_F16 && dtype != NVFP4_BF16)
     return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_quantize_append_paged: dtype must be NVFP4_F16 or NVFP4_BF16");
   if (nnz < 0) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_quantize_append_paged: nnz must be >= 0");
   if (batch_size < 0) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_quantize_append_paged: batch_size must be >= 0");
-  if (!(std::isfinite(k_scale) && k_scale > 0.0f) || !(std::isfinite(v_scale) && v_scale > 0.0f))
+  if (k_dev == nullptr &&
+      (!(std::isfinite(k_scale) && k_scale > 0.0f) || !(std::isfinite(v_scale) && v_scale > 0.0f)))
     return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_quantize_append_paged: k_scale and v_scale must be positive finite");
+  if (k_dev != nullptr && (v_dev == nullptr || !aligned(k_dev, 4) || !aligned(v_dev, 4)))
+    return fail(NVFP4_ERR_INVALID_ARG, std::string(fn) + ": k_scale and v_scale must be 4-byte aligned device pointers");
   if (nvfp4_status st = check_cache(fn, "k_cache", k_cache, page_size, num_kv_heads, head_dim)) return st;
   if (nvfp4_status st = check_cache(fn, "v_cache", v_cache, page_size, num_kv_heads, head_dim)) return st;
   if (nnz == 0) return NVFP4_OK;
@@ -208,6 +217,8 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_append_paged(
   a.batch_size = batch_size;
   a.gs[0] = k_scale;
   a.gs[1] = v_scale;
+  a.gs_dev[0] = k_dev;
+  a.gs_dev[1] = v_dev;
   a.cap_a = nvfp4_e4m3_max(recipe);
   a.neg_zero = 0x80000000u;
   a.status = dev_status;
@@ -216,6 +227,43 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_append_paged(
   const bool vec256 = aligned(append_key, 32) && aligned(append_value, 32) &&
                       key_row_stride % 16 == 0 && value_row_stride % 16 == 0;
   return launch_append(a, dtype == NVFP4_BF16, mode, vec256, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+NVFP4_EXPORT nvfp4_status nvfp4_quantize_append_paged(
+    const void* append_key, const void* append_value, int32_t dtype, int64_t nnz,
+    int32_t num_kv_heads, int32_t head_dim, int64_t key_row_stride, int64_t value_row_stride,
+    const int32_t* batch_indices, const int32_t* positions, nvfp4_paged_cache k_cache,
+    nvfp4_paged_cache v_cache, int32_t page_size, int32_t kv_layout,
+    const int32_t* kv_indices, int64_t num_kv_indices, const int32_t* kv_indptr,
+    const int32_t* kv_last_page_len, int32_t batch_size, float k_scale, float v_scale,
+    const nvfp4_4over6_config* recipe, int32_t* dev_status, void* stream) {
+  return append_impl("nvfp4_quantize_append_paged", append_key, append_value, dtype, nnz,
+                     num_kv_heads, head_dim, key_row_stride, value_row_stride, batch_indices,
+                     positions, k_cache, v_cache, page_size, kv_layout, kv_indices,
+                     num_kv_indices, kv_indptr, kv_last_page_len, batch_size, k_scale, v_scale,
+                     nullptr, nullptr, recipe, dev_status, stream);
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_quantize_append_paged_dev_scale(
+    const void* append_key, const void* append_value, int32_t dtype, int64_t nnz,
+    int32_t num_kv_heads, int32_t head_dim, int64_t key_row_stride, int64_t value_row_stride,
+    const int32_t* batch_indices, const int32_t* positions, nvfp4_paged_cache k_cache,
+    nvfp4_paged_cache v_cache, int32_t page_size, int32_t kv_layout,
+    const int32_t* kv_indices, int64_t num_kv_indices, const int32_t* kv_indptr,
+    const int32_t* kv_last_page_len, int32_t batch_size, const float* k_scale,
+    const float* v_scale, const nvfp4_4over6_config* recipe, int32_t* dev_status,
+    void* stream) {
+  if (k_scale == nullptr || v_scale == nullptr)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_quantize_append_paged_dev_scale: null scale pointer");
+  return append_impl("nvfp4_quantize_append_paged_dev_scale", append_key, append_value, dtype,
+                     nnz, num_kv_heads, head_dim, key_row_stride, value_row_stride,
+                     batch_indices, positions, k_cache, v_cache, page_size, kv_layout,
+                     kv_indices, num_kv_indices, kv_indptr, kv_last_page_len, batch_size, 1.0f,
+                     1.0f, k_scale, v_scale, recipe, dev_status, stream);
 }
 
 NVFP4_EXPORT nvfp4_status nvfp4_dequantize_paged(

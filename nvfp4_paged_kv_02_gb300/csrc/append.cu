@@ -277,6 +277,23 @@ __device__ __forceinline__ BlockOut quantize_block(const U32x8& in, const Tensor
   return r;
 }
 
+// The two global scales: from the arguments, or from device memory when given there.
+// Returns false (and reports it) when a device-held scale is not positive finite.
+__device__ __forceinline__ bool load_scales(const AppendArgs& a, float gs[2]) {
+  gs[0] = a.gs[0];
+  gs[1] = a.gs[1];
+  if (a.gs_dev[0] != nullptr) {
+    gs[0] = __ldg(a.gs_dev[0]);
+    gs[1] = __ldg(a.gs_dev[1]);
+    const bool ok = gs[0] > 0.0f && gs[0] <= FLT_MAX && gs[1] > 0.0f && gs[1] <= FLT_MAX;
+    if (!ok) {
+      if (threadIdx.x == 0 && blockIdx.x == 0) flag(a.status, NVFP4_DEV_BAD_SCALE);
+      return false;
+    }
+  }
+  return true;
+}
+
 // Fill the per-CTA tables for both tensors' global scales; ends with __syncthreads().
 __device__ __forceinline__ void fill_tables(Tables& tab, const float gs[2]) {
   for (int s = threadIdx.x; s < 256; s += blockDim.x) {
@@ -336,9 +353,11 @@ __device__ __forceinline__ RowMeta resolve_row(const AppendArgs& a, int64_t i) {
 template <bool BF16, int MODE, bool VEC256>
 __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   __shared__ Tables tab;
-  fill_tables(tab, a.gs);
-  const TensorConsts tck = make_consts(a.gs[0]);
-  const TensorConsts tcv = make_consts(a.gs[1]);
+  float gs[2];
+  if (!load_scales(a, gs)) return;
+  fill_tables(tab, gs);
+  const TensorConsts tck = make_consts(gs[0]);
+  const TensorConsts tcv = make_consts(gs[1]);
 
   const int64_t total = a.nnz * a.H * a.nb;
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -459,6 +478,8 @@ __global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const Append
   volatile uint32_t* s_issued = reinterpret_cast<uint32_t*>(smem + L.misc_off + 4);
   const int ns = L.ns;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float gs[2];
+  if (!load_scales(a, gs)) return;  // uniform over the CTA, before any barrier or copy
   if (threadIdx.x == 0) {
     for (int s = 0; s < ns; ++s) {
       mbar_init(full + s, 1);
@@ -468,7 +489,7 @@ __global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const Append
     *s_abort = 0;
     fence_mbar_init();
   }
-  fill_tables(tab, a.gs);  // ends with __syncthreads()
+  fill_tables(tab, gs);  // ends with __syncthreads()
 
   const int64_t tiles = (a.nnz + L.rows - 1) / L.rows;
   const uint32_t tile_bytes = L.rows * L.row_bytes;
@@ -518,8 +539,8 @@ __global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const Append
     }
   } else {
     const int ct = threadIdx.x;
-    const TensorConsts tck = make_consts(a.gs[0]);
-    const TensorConsts tcv = make_consts(a.gs[1]);
+    const TensorConsts tck = make_consts(gs[0]);
+    const TensorConsts tcv = make_consts(gs[1]);
     const int32_t row_blocks = a.H * a.nb;
     // step between heads of one row: codes, scales
     const int32_t hsd = a.layout == NVFP4_NHD ? a.D / 2 : a.ps * (a.D / 2);

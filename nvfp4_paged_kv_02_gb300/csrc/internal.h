@@ -49,6 +49,7 @@ struct AppendArgs {
   const int32_t* kv_last_page_len;
   int32_t batch_size;
   float gs[2];
+  const float* gs_dev[2];  // when set, the scales are read from device memory instead
   float cap_a;
   uint32_t neg_zero;  // 0x80000000 (-0.0f), passed at run time for fsq2_rn / hsq2_rn
   int32_t* status;

@@ -183,3 +183,12 @@ def test_ops_refuse_cpu_tensors():
     import torch
     with pytest.raises(ValueError):
         nv.nvfp4_make_global_scale(torch.zeros(16, dtype=torch.bfloat16))
+
+
+def test_dev_scale_append_rejects_null_scales(lib):
+    f = lib.nvfp4_quantize_append_paged_dev_scale
+    r = f(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 1, 4, 8, 128, 1024, 1024,
+          ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), cache(), cache(), 16, 0,
+          ctypes.c_void_p(FAKE), 16, ctypes.c_void_p(FAKE), None, 2, None, ctypes.c_void_p(FAKE),
+          None, None, None)
+    assert r == nv.ERR_INVALID_ARG and "scale" in err(lib)

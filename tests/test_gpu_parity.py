@@ -250,3 +250,44 @@ def test_global_scale(numel, dt):
         got = nv.nvfp4_make_global_scale(x.cuda(), recipe).item()
         want = O.global_scale(W.bits16(x), dt == torch.bfloat16, orecipe)
         assert np.float32(got).view(np.uint32) == np.float32(want).view(np.uint32), (got, want)
+
+
+def test_append_with_device_scales():
+    """The device-scale append writes exactly what the host-scale append writes; a device
+    scale that is not positive finite is reported and nothing is written."""
+    import nvfp4_paged_kv_02_gb300 as nv
+    dev = torch.device("cuda")
+    w = W.random_case(500, B=4, H=4, D=128, ps=16, layout=W.HND, dtype=torch.bfloat16,
+                      recipe=R_MAE16, max_len=80)
+    t = lambda a: torch.as_tensor(np.ascontiguousarray(a)).to(dev)
+    r = PL.gpu_recipe(w.recipe)
+    outs = []
+    for use_dev in (False, True):
+        kd = torch.full((w.num_pages, w.H, w.ps, w.D // 2), 0xA5, dtype=torch.uint8, device=dev)
+        ks = torch.full((w.num_pages, w.H, w.ps, w.D // 16), 0xA5, dtype=torch.uint8, device=dev)
+        vd, vs = kd.clone(), ks.clone()
+        gk = nv.nvfp4_make_global_scale(w.k.to(dev), r)
+        gv = nv.nvfp4_make_global_scale(w.v.to(dev), r)
+        sk, sv = (gk, gv) if use_dev else (gk.item(), gv.item())
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        nv.nvfp4_quantize_append_paged(w.k.to(dev), w.v.to(dev), t(w.batch_indices),
+                                       t(w.positions), (kd, vd), (ks, vs), t(w.kv_indices),
+                                       t(w.kv_indptr), t(w.kv_last_page_len), sk, sv, "HND", r, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        outs.append([x.cpu().numpy() for x in (kd, ks, vd, vs)])
+    for a, b in zip(*outs):
+        assert np.array_equal(a, b)
+    for bad in (0.0, -1.0, float("inf"), float("nan")):
+        kd = torch.full((w.num_pages, w.H, w.ps, w.D // 2), 0xA5, dtype=torch.uint8, device=dev)
+        ks = torch.full((w.num_pages, w.H, w.ps, w.D // 16), 0xA5, dtype=torch.uint8, device=dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        g_bad = torch.tensor([bad], dtype=torch.float32, device=dev)
+        g_ok = torch.tensor([0.01], dtype=torch.float32, device=dev)
+        nv.nvfp4_quantize_append_paged(w.k.to(dev), w.v.to(dev), t(w.batch_indices),
+                                       t(w.positions), (kd, kd.clone()), (ks, ks.clone()),
+                                       t(w.kv_indices), t(w.kv_indptr), None, g_ok, g_bad, "HND",
+                                       r, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == nv.DEV_BAD_SCALE
+        assert (kd == 0xA5).all() and (ks == 0xA5).all()
