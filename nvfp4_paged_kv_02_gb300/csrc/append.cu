@@ -60,47 +60,23 @@ __device__ __forceinline__ float quotient(float a, float b, float rb, bool exact
   return exact_rcp ? div_rn_with_rcp(a, b, rb) : __fdiv_rn(a, b);
 }
 
+// Exact binary32 values of the 16 elements. For bf16 the low half is widened with an
+// integer multiply by 2^16 (the FMA pipe) rather than a shift (the half-rate ALU pipe,
+// which the E2M1 decodes already keep busy).
 template <bool BF16>
 __device__ __forceinline__ void unpack16(const U32x8& in, float x[16]) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     if (BF16) {
-      x[2 * k] = f32_from_bf16_lo(in.w[k]);
+      uint32_t lo;
+      asm("mul.lo.u32 %0, %1, 65536;" : "=r"(lo) : "r"(in.w[k]));
+      x[2 * k] = __uint_as_float(lo);
       x[2 * k + 1] = f32_from_bf16_hi(in.w[k]);
     } else {
       x[2 * k] = f32_from_f16_lo(in.w[k]);
       x[2 * k + 1] = f32_from_f16_hi(in.w[k]);
     }
   }
-}
-
-// max |x| of the block, exactly, from the packed words: packed maxima of magnitudes
-// (max.xorsign.abs keeps |.| in bits 14:0 of each half), then the larger half.
-template <bool BF16>
-__device__ __forceinline__ float block_amax(const U32x8& in) {
-  uint32_t m[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    if (BF16)
-      asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m[k]) : "r"(in.w[2 * k]), "r"(in.w[2 * k + 1]));
-    else
-      asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(m[k]) : "r"(in.w[2 * k]), "r"(in.w[2 * k + 1]));
-  }
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    if (BF16)
-      asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m[k]) : "r"(m[k]), "r"(m[k + 2]));
-    else
-      asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(m[k]) : "r"(m[k]), "r"(m[k + 2]));
-  }
-  uint32_t t;
-  if (BF16)
-    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(t) : "r"(m[0]), "r"(m[1]));
-  else
-    asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(t) : "r"(m[0]), "r"(m[1]));
-  const uint32_t mag = max(t & 0x7FFFu, (t >> 16) & 0x7FFFu);  // magnitudes order like ints
-  return BF16 ? __uint_as_float(mag << 16)
-              : __half2float(__ushort_as_half(static_cast<unsigned short>(mag)));
 }
 
 // Four element pairs (x[0..7]) with multiplier inv: the four code bytes, and the decoded
@@ -243,7 +219,10 @@ __device__ __forceinline__ BlockOut quantize_block(const U32x8& in, const Tensor
                                                    uint32_t nz) {
   float x[16];
   unpack16<BF16>(in, x);
-  const float amax = block_amax<BF16>(in);
+  // max |x| with the absolute value folded into the max (which issues on the FMA pipe)
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
   const float ra = fminf(quotient(amax, tc.g6, tc.r6, tc.exact_rcp), cap_a);
   BlockOut r;
   if (MODE == 0) {
@@ -255,7 +234,10 @@ __device__ __forceinline__ BlockOut quantize_block(const U32x8& in, const Tensor
   }
   const float rb = fminf(quotient(amax, tc.g4, tc.r4, tc.exact_rcp), 448.0f);
   const uint32_t sab = e4m3x2_from_f32(ra, rb);
-  const uint32_t sa = sab & 0xFFu, sb = sab >> 8;
+  // sb = sab >> 8 and sa = sab & 0xFF as multiplies (FMA pipe)
+  uint32_t sb;
+  asm("mul.hi.u32 %0, %1, 16777216;" : "=r"(sb) : "r"(sab));
+  const uint32_t sa = sab - sb * 256u;
   uint32_t a0, a1, b0, b1;
   float ea, eb;
   if (MODE == 1 || MODE == 2) {
