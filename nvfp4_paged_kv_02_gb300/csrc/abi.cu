@@ -3,6 +3,7 @@
 // alignment and shared extents -- plus the scale values passed by value), then one
 // launch sequence on the caller's stream.
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <sstream>
@@ -40,6 +41,12 @@ int current_device() {
   return dev;
 }
 }  // namespace
+
+PipeTest pipe_test_from_env() {
+  const char* v = std::getenv("NVFP4KV_TEST_STALL_PIPELINE");
+  if (v != nullptr && v[0] == '1') return PipeTest{1u << 12, 1};
+  return PipeTest{kWaitLimit, 0};
+}
 
 int sm_count() {
   const int dev = current_device();
@@ -221,6 +228,7 @@ nvfp4_status append_impl(
   a.gs_dev[1] = v_dev;
   a.cap_a = nvfp4_e4m3_max(recipe);
   a.neg_zero = 0x80000000u;
+  a.pipe = pipe_test_from_env();
   a.status = dev_status;
   int mode = 0;
   if (recipe) mode = 1 + (recipe->err_mode == NVFP4_ERR_MSE ? 1 : 0) + (recipe->err_use_fast_math ? 2 : 0);
@@ -301,6 +309,7 @@ NVFP4_EXPORT nvfp4_status nvfp4_dequantize_paged(
   a.layout = kv_layout;
   a.div_row_blocks = make_div(static_cast<int64_t>(num_kv_heads) * a.nb);
   a.div_nb = make_div(a.nb);
+  a.div_ps = make_div(page_size);
   a.block_tables = block_tables;
   a.max_pages = max_pages_per_request;
   a.seq_lens = seq_lens;
@@ -310,6 +319,7 @@ NVFP4_EXPORT nvfp4_status nvfp4_dequantize_paged(
   a.out_k = static_cast<uint8_t*>(output_k);
   a.out_v = static_cast<uint8_t*>(output_v);
   a.L = max_seq_len;
+  a.pipe = pipe_test_from_env();
   a.status = dev_status;
   const bool vec256 = aligned(output_k, 32) && aligned(output_v, 32);
   return launch_dequant(a, out_dtype == NVFP4_BF16, table_dtype == NVFP4_I64, vec256,
@@ -388,6 +398,7 @@ NVFP4_EXPORT nvfp4_status nvfp4_materialize_fp8(
   a.out_num_pages = out_num_pages;
   a.tables = fp8_block_tables;
   a.zero_tables = zero_fp8_block_tables ? 1 : 0;
+  a.pipe = pipe_test_from_env();
   a.status = dev_status;
   if (batch_size == 0) {
     // nothing active: the copy is just its zero page

@@ -481,7 +481,7 @@ __global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const Append
     uint32_t phase = 0, round = 0;  // phase = parity of `round`, the stage's fill count
     for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
       bool ok = true;
-      if (lane == 0) ok = mbar_wait(empty + s, phase ^ 1u) && !*s_abort;
+      if (lane == 0) ok = mbar_wait(empty + s, phase ^ 1u, a.pipe.wait_limit) && !*s_abort;
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) {
         if (lane == 0) {
@@ -490,17 +490,19 @@ __global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const Append
         }
         break;
       }
+      // (test control: withhold the first stage so that the consumers' wait expires)
+      const bool withhold = a.pipe.stall && round == 0 && s == 0;
       uint8_t* st = stages + static_cast<uint32_t>(s) * L.stage_bytes;
       RowDst* dst = reinterpret_cast<RowDst*>(st + 2u * tile_bytes);
       const int64_t row0 = tile * L.rows;
-      const uint32_t nrows =
-          static_cast<uint32_t>(min(static_cast<int64_t>(L.rows), a.nnz - row0));
+      const uint32_t nrows = withhold ? 0u
+          : static_cast<uint32_t>(min(static_cast<int64_t>(L.rows), a.nnz - row0));
       for (uint32_t r = lane; r < nrows; r += 32) dst[r] = resolve_row_dst(a, row0 + r);
       __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(full + s, 2u * nrows * L.row_bytes);
+      if (lane == 0 && !withhold) mbar_arrive_expect_tx(full + s, 2u * nrows * L.row_bytes);
       __syncwarp();
       if (contiguous) {
-        if (lane == 0) {
+        if (lane == 0 && nrows > 0) {
           bulk_g2s(st, a.k + row0 * a.k_row_bytes, nrows * L.row_bytes, full + s);
           bulk_g2s(st + tile_bytes, a.v + row0 * a.v_row_bytes, nrows * L.row_bytes, full + s);
         }
@@ -511,7 +513,7 @@ __global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const Append
                    L.row_bytes, full + s);
         }
       }
-      if (lane == 0) s_issued[s] = round + 1;
+      if (lane == 0 && !withhold) s_issued[s] = round + 1;
       __syncwarp();
       if (++s == ns) {
         s = 0;
@@ -530,7 +532,7 @@ __global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const Append
     int s = 0;
     uint32_t phase = 0;
     for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
-      if (*s_abort || !mbar_wait(full + s, phase)) {
+      if (*s_abort || !mbar_wait(full + s, phase, a.pipe.wait_limit)) {
         if (lane == 0) {
           *s_abort = 1;
           flag(a.status, NVFP4_DEV_TIMEOUT);
@@ -573,7 +575,7 @@ __global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const Append
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int s = 0; s < ns; ++s)
-      if (s_issued[s] > 0) mbar_wait(full + s, (s_issued[s] - 1) & 1u);
+      if (s_issued[s] > 0) mbar_wait(full + s, (s_issued[s] - 1) & 1u, a.pipe.wait_limit);
   }
 }
 

@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) dequant_tma_kernel(const Dequa
     for (int64_t item = blockIdx.x; item < items;
          item += gridDim.x, s = (s + 1 == ns) ? 0 : s + 1, round += (s == 0)) {
       bool ok = true;
-      if (lane == 0) ok = mbar_wait(empty + s, (round & 1u) ^ 1u) && !*s_abort;
+      if (lane == 0) ok = mbar_wait(empty + s, (round & 1u) ^ 1u, a.pipe.wait_limit) && !*s_abort;
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) {
         if (lane == 0) {
@@ -181,7 +181,8 @@ __global__ void __launch_bounds__(kTmaThreads, 2) dequant_tma_kernel(const Dequa
         }
         break;
       }
-      if (lane == 0) {
+      // (test control: withhold the first stage so that the consumers' wait expires)
+      if (lane == 0 && !(a.pipe.stall && round == 0 && s == 0)) {
         const int kv = static_cast<int>(item & 1);
         const int32_t pi = static_cast<int32_t>(item >> 1);
         const int32_t b = scan_find(s_cum, a.B, pi);
@@ -226,7 +227,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) dequant_tma_kernel(const Dequa
     uint32_t round = 0;  // how many times stage s has been used before
     for (int64_t item = blockIdx.x; item < items;
          item += gridDim.x, s = (s + 1 == ns) ? 0 : s + 1, round += (s == 0)) {
-      if (*s_abort || !mbar_wait(full + s, round & 1u)) {
+      if (*s_abort || !mbar_wait(full + s, round & 1u, a.pipe.wait_limit)) {
         if (lane == 0) {
           *s_abort = 1;
           flag(a.status, NVFP4_DEV_TIMEOUT);
@@ -240,19 +241,30 @@ __global__ void __launch_bounds__(kTmaThreads, 2) dequant_tma_kernel(const Dequa
         uint8_t* ob = ((m.flags & 1) ? a.out_v : a.out_k) +
                       (static_cast<int64_t>(m.f0) * L_out + m.f1) * row_bytes;
         const float gs = (m.flags & 1) ? gs_v : gs_k;
-        const int32_t nblk = m.f2 * row_blocks;
+        const int32_t ntok = m.f2;
+        if (a.layout == NVFP4_NHD) {
+          // the page holds [slot, head, block]: the same order as the output run
+          const int32_t nblk = ntok * row_blocks;
 #pragma unroll 4
-        for (int32_t k = ct; k < nblk; k += kConsumers) {
-          int32_t off = k;  // NHD: block index inside the page equals k
-          if (a.layout == NVFP4_HND) {
-            const int32_t slot = static_cast<int32_t>(div_q(k, a.div_row_blocks));
-            const int32_t rem = k - slot * row_blocks;
-            const int32_t h = static_cast<int32_t>(div_q(rem, a.div_nb));
-            off = (h * ps + slot) * a.nb + (rem - h * a.nb);
+          for (int32_t k = ct; k < nblk; k += kConsumers) {
+            const uint2 codes = *reinterpret_cast<const uint2*>(st + 8 * k);
+            st_256(ob + static_cast<int64_t>(k) * 32, decode_block<OUT_BF16>(codes, sfp[k], gs));
           }
-          const uint2 codes = *reinterpret_cast<const uint2*>(st + 8 * off);
-          const U32x8 o = decode_block<OUT_BF16>(codes, sfp[off], gs);
-          st_256(ob + static_cast<int64_t>(k) * 32, o);
+        } else {
+          // the page holds [head, slot, block]: read it in that order (no shared-memory
+          // bank conflicts); each group of nb lanes still writes a contiguous output row
+          const int32_t page_blocks = a.H * ps * a.nb;
+#pragma unroll 4
+          for (int32_t k = ct; k < page_blocks; k += kConsumers) {
+            const int32_t hs = div_q32(k, a.div_nb);  // h * ps + slot
+            const int32_t blk = k - hs * a.nb;
+            const int32_t h = div_q32(hs, a.div_ps);
+            const int32_t slot = hs - h * ps;
+            if (slot >= ntok) continue;
+            const uint2 codes = *reinterpret_cast<const uint2*>(st + 8 * k);
+            const int32_t o = (slot * a.H + h) * a.nb + blk;
+            st_256(ob + static_cast<int64_t>(o) * 32, decode_block<OUT_BF16>(codes, sfp[k], gs));
+          }
         }
       }
       __syncwarp();
@@ -263,7 +275,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) dequant_tma_kernel(const Dequa
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int s = 0; s < ns; ++s)
-      if (s_issued[s] > 0) mbar_wait(full + s, (s_issued[s] - 1) & 1u);
+      if (s_issued[s] > 0) mbar_wait(full + s, (s_issued[s] - 1) & 1u, a.pipe.wait_limit);
   }
 }
 

@@ -8,6 +8,7 @@
 
 #include "../../include/nvfp4kv.h"
 #include "device.cuh"
+#include "pipeline.cuh"
 
 #define NVFP4_EXPORT __attribute__((visibility("default")))
 
@@ -25,6 +26,9 @@ int sm_count();
 // Resident CTAs per SM for `kernel` at `threads` threads and `smem` dynamic bytes
 // (cached per kernel and device).
 int blocks_per_sm(const void* kernel, int threads, size_t smem);
+
+// Pipeline test control from the environment (NVFP4KV_TEST_STALL_PIPELINE=1).
+PipeTest pipe_test_from_env();
 
 // Largest batch the page-scan kernels keep in shared memory (one int32 per request).
 constexpr int kMaxScanBatch = 16384;
@@ -52,6 +56,7 @@ struct AppendArgs {
   const float* gs_dev[2];  // when set, the scales are read from device memory instead
   float cap_a;
   uint32_t neg_zero;  // 0x80000000 (-0.0f), passed at run time for fsq2_rn / hsq2_rn
+  PipeTest pipe;
   int32_t* status;
 };
 // mode: 0 standard NVFP4; 1/2 4over6 binary32 MAE/MSE; 3/4 4over6 binary16 MAE/MSE.
@@ -62,7 +67,7 @@ nvfp4_status launch_append(const AppendArgs& a, bool bf16, int mode, bool vec256
 struct DequantArgs {
   nvfp4_paged_cache kc, vc;
   int32_t ps, H, D, nb, layout;
-  Div div_row_blocks, div_nb;
+  Div div_row_blocks, div_nb, div_ps;
   const void* block_tables;
   int64_t max_pages;
   const int32_t* seq_lens;
@@ -72,6 +77,7 @@ struct DequantArgs {
   uint8_t* out_k;
   uint8_t* out_v;
   int32_t L;
+  PipeTest pipe;
   int32_t* status;
 };
 nvfp4_status launch_dequant(const DequantArgs& a, bool out_bf16, bool bt64, bool vec256,
@@ -93,6 +99,7 @@ struct MaterializeArgs {
   int64_t out_num_pages;
   int32_t* tables;
   int32_t zero_tables;
+  PipeTest pipe;
   int32_t* status;
 };
 nvfp4_status launch_materialize(const MaterializeArgs& a, cudaStream_t stream);

@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) materialize_tma_kernel(const M
     for (int64_t item = blockIdx.x; item < items;
          item += gridDim.x, s = (s + 1 == ns) ? 0 : s + 1, round += (s == 0)) {
       bool ok = true;
-      if (lane == 0) ok = mbar_wait(empty + s, (round & 1u) ^ 1u) && !*s_abort;
+      if (lane == 0) ok = mbar_wait(empty + s, (round & 1u) ^ 1u, a.pipe.wait_limit) && !*s_abort;
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) {
         if (lane == 0) {
@@ -209,7 +209,8 @@ __global__ void __launch_bounds__(kTmaThreads, 2) materialize_tma_kernel(const M
         }
         break;
       }
-      if (lane == 0) {
+      // (test control: withhold the first stage so that the consumers' wait expires)
+      if (lane == 0 && !(a.pipe.stall && round == 0 && s == 0)) {
         const int kv = static_cast<int>(item & 1);
         const int32_t pi = static_cast<int32_t>(item >> 1);
         const int32_t b = scan_find(s_cum, a.B, pi);
@@ -255,7 +256,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) materialize_tma_kernel(const M
     uint32_t round = 0;  // how many times stage s has been used before
     for (int64_t item = blockIdx.x; item < items;
          item += gridDim.x, s = (s + 1 == ns) ? 0 : s + 1, round += (s == 0)) {
-      if (*s_abort || !mbar_wait(full + s, round & 1u)) {
+      if (*s_abort || !mbar_wait(full + s, round & 1u, a.pipe.wait_limit)) {
         if (lane == 0) {
           *s_abort = 1;
           flag(a.status, NVFP4_DEV_TIMEOUT);
@@ -288,7 +289,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) materialize_tma_kernel(const M
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int s = 0; s < ns; ++s)
-      if (s_issued[s] > 0) mbar_wait(full + s, (s_issued[s] - 1) & 1u);
+      if (s_issued[s] > 0) mbar_wait(full + s, (s_issued[s] - 1) & 1u, a.pipe.wait_limit);
   }
 }
 

@@ -54,12 +54,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase of parity `parity` to complete; false after kWaitLimit polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
+// Wait for the phase of parity `parity` to complete; false after `limit` polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint32_t limit = kWaitLimit) {
+  for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
+
+// Test control of a pipelined launch: `stall` makes the producer withhold the first stage
+// of each CTA (so the consumers' wait expires), with a short `wait_limit`.
+struct PipeTest {
+  uint32_t wait_limit;
+  int32_t stall;
+};
 
 // Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from global to
 // this CTA's shared memory, completing as transaction bytes on `bar`.
