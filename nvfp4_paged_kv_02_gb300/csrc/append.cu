@@ -80,13 +80,14 @@ __device__ __forceinline__ void unpack16(const U32x8& in, float x[16]) {
 }
 
 // Four element pairs (x[0..7]) with multiplier inv: the four code bytes, and the decoded
-// values e2m1(q) as four half2.
+// values e2m1(q) as four half2. The decodes read the bytes of the packed word (which takes
+// fewer integer instructions than decoding each conversion result).
 __device__ __forceinline__ uint32_t encode8(const float* x, float inv, uint32_t v[4]) {
   uint32_t code;
   asm("{\n\t"
       ".reg .b64 ip, p0, p1, p2, p3;\n\t"
       ".reg .f32 y0, y1, y2, y3, y4, y5, y6, y7;\n\t"
-      ".reg .b8 q0, q1, q2, q3;\n\t"
+      ".reg .b8 q0, q1, q2, q3, r0, r1, r2, r3;\n\t"
       "mov.b64 ip, {%5, %5};\n\t"
       "mov.b64 p0, {%6, %7};\n\t"
       "mov.b64 p1, {%8, %9};\n\t"
@@ -104,11 +105,12 @@ __device__ __forceinline__ uint32_t encode8(const float* x, float inv, uint32_t 
       "cvt.rn.satfinite.e2m1x2.f32 q1, y3, y2;\n\t"
       "cvt.rn.satfinite.e2m1x2.f32 q2, y5, y4;\n\t"
       "cvt.rn.satfinite.e2m1x2.f32 q3, y7, y6;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %1, q0;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %2, q1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %3, q2;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %4, q3;\n\t"
       "mov.b32 %0, {q0, q1, q2, q3};\n\t"
+      "mov.b32 {r0, r1, r2, r3}, %0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, r0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, r1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, r2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %4, r3;\n\t"
       "}"
       : "=r"(code), "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
       : "f"(inv), "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]),
@@ -480,6 +482,15 @@ __global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const Append
     int s = 0;
     uint32_t phase = 0, round = 0;  // phase = parity of `round`, the stage's fill count
     for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+      // (test control: withhold the first stage so that the consumers' wait expires)
+      const bool withhold = a.pipe.stall && round == 0 && s == 0;
+      const int64_t row0 = tile * L.rows;
+      const uint32_t nrows = withhold ? 0u
+          : static_cast<uint32_t>(min(static_cast<int64_t>(L.rows), a.nnz - row0));
+      // Resolve this tile's destinations (a chain of dependent index loads, one row per
+      // lane: at most 32 rows) while the consumers still work on the stage it will use.
+      RowDst d{nullptr, nullptr, nullptr, nullptr};
+      if (static_cast<uint32_t>(lane) < nrows) d = resolve_row_dst(a, row0 + lane);
       bool ok = true;
       if (lane == 0) ok = mbar_wait(empty + s, phase ^ 1u, a.pipe.wait_limit) && !*s_abort;
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -490,14 +501,9 @@ __global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const Append
         }
         break;
       }
-      // (test control: withhold the first stage so that the consumers' wait expires)
-      const bool withhold = a.pipe.stall && round == 0 && s == 0;
       uint8_t* st = stages + static_cast<uint32_t>(s) * L.stage_bytes;
       RowDst* dst = reinterpret_cast<RowDst*>(st + 2u * tile_bytes);
-      const int64_t row0 = tile * L.rows;
-      const uint32_t nrows = withhold ? 0u
-          : static_cast<uint32_t>(min(static_cast<int64_t>(L.rows), a.nnz - row0));
-      for (uint32_t r = lane; r < nrows; r += 32) dst[r] = resolve_row_dst(a, row0 + r);
+      if (static_cast<uint32_t>(lane) < nrows) dst[lane] = d;
       __syncwarp();
       if (lane == 0 && !withhold) mbar_arrive_expect_tx(full + s, 2u * nrows * L.row_bytes);
       __syncwarp();
@@ -506,12 +512,11 @@ __global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const Append
           bulk_g2s(st, a.k + row0 * a.k_row_bytes, nrows * L.row_bytes, full + s);
           bulk_g2s(st + tile_bytes, a.v + row0 * a.v_row_bytes, nrows * L.row_bytes, full + s);
         }
-      } else {
-        for (uint32_t r = lane; r < nrows; r += 32) {
-          bulk_g2s(st + r * L.row_bytes, a.k + (row0 + r) * a.k_row_bytes, L.row_bytes, full + s);
-          bulk_g2s(st + tile_bytes + r * L.row_bytes, a.v + (row0 + r) * a.v_row_bytes,
-                   L.row_bytes, full + s);
-        }
+      } else if (static_cast<uint32_t>(lane) < nrows) {
+        const uint32_t r = lane;
+        bulk_g2s(st + r * L.row_bytes, a.k + (row0 + r) * a.k_row_bytes, L.row_bytes, full + s);
+        bulk_g2s(st + tile_bytes + r * L.row_bytes, a.v + (row0 + r) * a.v_row_bytes,
+                 L.row_bytes, full + s);
       }
       if (lane == 0 && !withhold) s_issued[s] = round + 1;
       __syncwarp();
@@ -592,8 +597,8 @@ nvfp4_status launch_t(const AppendArgs& a, cudaStream_t stream) {
   return check_launch("nvfp4_quantize_append_paged");
 }
 
-// TMA path: tiles of up to 32 rows and about 16 KB per tensor, 2 to 6 stages in 70 KB
-// (three CTAs per SM).
+// TMA path: tiles of up to 32 rows (the producer gives each row one lane) and about 16 KB
+// per tensor, 2 to 6 stages in 70 KB (three CTAs per SM).
 template <bool BF16, int MODE>
 nvfp4_status launch_tma(const AppendArgs& a, uint32_t row_bytes, cudaStream_t stream) {
   const auto kern = append_tma_kernel<BF16, MODE>;
