@@ -21,6 +21,7 @@ shards by request with no exchange): weak scaling, max time over ranks.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -66,6 +67,46 @@ def op_bytes(w: W.Workload, n_active_pages: int):
         + w.B * (-(-w.max_kv_len // ps)) * 4,
     }, {"global_scale": nnz, "append": nnz, "dequant_paged": toks,
         "materialize": n_active_pages * ps}
+
+
+# ---------------------------------------------------------------------------------------
+# DRAM traffic of a kernel, from a committed ncu summary
+# ---------------------------------------------------------------------------------------
+
+CSRC = os.path.join(ROOT, "nvfp4_paged_kv_02_gb300", "csrc")
+KERNEL_SOURCES = {
+    "append": ["append.cu"], "dequant_paged": ["dequant.cu"],
+    "materialize": ["materialize.cu"],
+}
+SHARED_SOURCES = ["device.cuh", "internal.h", "pipeline.cuh", "scan.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic_large_pool.md")
+
+
+def source_hash(op: str) -> str:
+    """First 16 hex digits of the sha256 of the op's translation unit and shared headers."""
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[op] + SHARED_SOURCES:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_per_launch(op: str, units: int):
+    """DRAM bytes (read + write) per launch of the op's kernel: the bytes per unit that an ncu
+    capture measured, times the units of this launch. None when there is no capture or the
+    kernel's sources changed since it was taken."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    want = source_hash(op)
+    with open(TRAFFIC_FILE) as f:
+        for ln in f:
+            cells = [c.strip().strip("`") for c in ln.strip().strip("|").split("|")]
+            if len(cells) >= 6 and cells[0] == op and cells[1] == want:
+                try:
+                    return float(cells[5]) * units
+                except ValueError:
+                    return None
+    return None
 
 
 # ---------------------------------------------------------------------------------------
@@ -406,7 +447,7 @@ def main():
                          "achieved": nbytes[dom] / (op_ms[dom] * 1e-3) / 1e9,
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": nbytes[dom] / (op_ms[dom] * 1e-3) / 1e9 / peak,
-                         "traffic": None},
+                         "traffic": traffic_per_launch(dom, ntok[dom])},
             "clocks": clk, "gpu_launches": step.launches_per_step * args.steps,
             "e2e": e2e, "cpu_baseline": cpu, "device_status": status,
         }

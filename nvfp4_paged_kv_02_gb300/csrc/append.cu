@@ -534,6 +534,12 @@ __global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const Append
     // step between heads of one row: codes, scales
     const int32_t hsd = a.layout == NVFP4_NHD ? a.D / 2 : a.ps * (a.D / 2);
     const int32_t hss = a.layout == NVFP4_NHD ? a.nb : a.ps * a.nb;
+    // when a row's blocks divide the consumer count, each thread keeps one (head, block)
+    const bool fixed = kConsumers % row_blocks == 0;
+    const int32_t fr0 = fixed ? ct / row_blocks : 0, frs = fixed ? kConsumers / row_blocks : 0;
+    const int32_t frem = fixed ? ct - fr0 * row_blocks : 0;
+    const int32_t fh = fixed ? frem / a.nb : 0, fj = fixed ? frem - fh * a.nb : 0;
+    const int32_t fod = fh * hsd + 8 * fj, fos = fh * hss + fj;
     int s = 0;
     uint32_t phase = 0;
     for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
@@ -549,14 +555,17 @@ __global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const Append
       const int32_t nrows =
           static_cast<int32_t>(min(static_cast<int64_t>(L.rows), a.nnz - tile * L.rows));
       const int32_t nblk = nrows * row_blocks;
-      for (int32_t k = ct; k < nblk; k += kConsumers) {
-        const int32_t r = div_q32(k, a.div_row_blocks);
-        const int32_t rem = k - r * row_blocks;
-        const int32_t h = div_q32(rem, a.div_nb);
-        const int32_t j = rem - h * a.nb;
+      for (int32_t k = ct, rf = fr0; k < nblk; k += kConsumers, rf += frs) {
+        int32_t r = rf, od = fod, os = fos;
+        if (!fixed) {
+          r = div_q32(k, a.div_row_blocks);
+          const int32_t rem = k - r * row_blocks;
+          const int32_t h = div_q32(rem, a.div_nb);
+          const int32_t j = rem - h * a.nb;
+          od = h * hsd + 8 * j;
+          os = h * hss + j;
+        }
         const RowDst d = dst[r];
-        const int32_t od = h * hsd + 8 * j;
-        const int32_t os = h * hss + j;
 #pragma unroll
         for (int kv = 0; kv < 2; ++kv) {
           uint8_t* pd = kv ? d.vd : d.kd;
