@@ -113,6 +113,10 @@ def load(path: str):
     L.oracle_materialize_fp8.argtypes = (
         [vp, vp, i64, i64, vp, vp, i64, i64, i32, i32, i32, i32, vp, i32, i32, vp,
          i32, i32, vp, vp, vp, i32, i32])
+    L.oracle_kv_quantize.restype = None
+    L.oracle_kv_quantize.argtypes = [vp, i32, i64, i64, i64, f32, vp, vp, vp, i32]
+    L.oracle_kv_dequantize.restype = None
+    L.oracle_kv_dequantize.argtypes = [vp, vp, i64, i64, f32, vp, i32, i32]
     L.oracle_max_threads.restype = i32
     L.oracle_max_threads.argtypes = []
     return L
@@ -279,3 +283,31 @@ def materialize_fp8(kc: PagedCache, vc: PagedCache, ps: int, H: int, D: int, lay
         _p(vc.data), _p(vc.sf), vc.data_page_stride, vc.sf_page_stride,
         ps, H, D, layout, _p(bt), mnp, int(shared), _p(sl), sl.size, max_kv_len, _p(ip),
         _p(out), _p(fp8_block_tables), int(zero_tables), nthreads or max_threads())
+
+
+def kv_quantize(x_bits: np.ndarray, is_bf16: bool, gs: float, recipe: Optional[Recipe] = None,
+                nthreads: int = 0):
+    """Contiguous quantize of uint16 bits [..., cols] (rows = the product of the leading
+    dimensions): returns (codes uint8 [..., cols/2], scales uint8 [..., cols/16])."""
+    x = np.ascontiguousarray(x_bits, np.uint16)
+    cols = x.shape[-1]
+    rows = x.size // cols if cols else 0
+    codes = np.zeros(x.shape[:-1] + (cols // 2,), np.uint8)
+    sf = np.zeros(x.shape[:-1] + (cols // 16,), np.uint8)
+    lib().oracle_kv_quantize(_p(x), int(is_bf16), rows, cols, cols, gs, _recipe_ptr(recipe),
+                             _p(codes), _p(sf), nthreads or max_threads())
+    return codes, sf
+
+
+def kv_dequantize(codes: np.ndarray, sf: np.ndarray, gs: float, out_bf16: bool,
+                  nthreads: int = 0) -> np.ndarray:
+    """Contiguous dequantize: codes uint8 [..., cols/2], scales uint8 [..., cols/16] ->
+    uint16 bits [..., cols] of the output type."""
+    c = np.ascontiguousarray(codes, np.uint8)
+    s = np.ascontiguousarray(sf, np.uint8)
+    cols = 2 * c.shape[-1]
+    rows = c.size // c.shape[-1] if c.shape[-1] else 0
+    out = np.zeros(c.shape[:-1] + (cols,), np.uint16)
+    lib().oracle_kv_dequantize(_p(c), _p(s), rows, cols, gs, _p(out), int(out_bf16),
+                               nthreads or max_threads())
+    return out

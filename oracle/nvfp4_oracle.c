@@ -12,6 +12,8 @@
  *        -- parameters, returns, note.
  *   [P4] "flashinfer.quantization" API index -- "NVFP4 4over6 Recipes" section,
  *        "Precedence" note, "NVFP4KVMaterializer" class.
+ *   [P5] "flashinfer.quantization" API index -- "FP4 KV Cache Quantization" section:
+ *        nvfp4_kv_quantize / nvfp4_kv_dequantize (contiguous, linear block-scale layout).
  *
  * Conventions the pages leave open, fixed here (each is one reading, stated where used):
  *   - E2M1 grid {0,0.5,1,1.5,2,3,4,6}, round-to-nearest-even, saturating at 6, sign kept
@@ -506,4 +508,43 @@ ORACLE_API int32_t oracle_max_threads(void) {
 #else
   return 1;
 #endif
+}
+
+/* ------------------------------------------------------------------------------------- */
+/* Contiguous quantize and dequantize ([P5]).                                            */
+/* ------------------------------------------------------------------------------------- */
+
+/* nvfp4_kv_quantize: the same per-block rule as the append, on a plain [rows, cols] tensor
+ * (any leading dimensions flattened into rows). Reading: output codes [rows, cols/2] and
+ * scales [rows, cols/16], both row-major, i.e. the linear block-scale layout the section
+ * names; the recipe applies as for every NVFP4 entry point ([P4], "Precedence"). */
+ORACLE_API void oracle_kv_quantize(const uint16_t* x, int is_bf16, int64_t rows, int64_t cols,
+                                   int64_t row_stride, float gs, const oracle_recipe* r,
+                                   uint8_t* codes, uint8_t* sf, int32_t nthreads) {
+  (void)nthreads;
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+  for (int64_t i = 0; i < rows; ++i) {
+    for (int64_t j = 0; j < cols / 16; ++j) {
+      float xb[16];
+      for (int k = 0; k < 16; ++k) xb[k] = in_value(x, i * row_stride + 16 * j + k, is_bf16);
+      quantize_block(xb, gs, r, codes + i * (cols / 2) + 8 * j, sf + i * (cols / 16) + j, NULL,
+                     NULL);
+    }
+  }
+}
+
+/* nvfp4_kv_dequantize: every element of the [rows, cols] codes decodes with its block's
+ * scale and the global scale, exactly as a paged dequant ([P2] decode rule). */
+ORACLE_API void oracle_kv_dequantize(const uint8_t* codes, const uint8_t* sf, int64_t rows,
+                                     int64_t cols, float gs, uint16_t* out, int32_t out_bf16,
+                                     int32_t nthreads) {
+  (void)nthreads;
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+  for (int64_t i = 0; i < rows; ++i) {
+    for (int64_t d = 0; d < cols; ++d) {
+      uint32_t byte = codes[i * (cols / 2) + d / 2];
+      uint32_t code = (d % 2 == 0) ? (byte & 0xFu) : (byte >> 4);
+      out[i * cols + d] = dequant_value(code, sf[i * (cols / 16) + d / 16], gs, out_bf16);
+    }
+  }
 }

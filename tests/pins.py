@@ -728,10 +728,87 @@ def pin_dequant_multiplication_order(O):
             assert out_k[0, 0, 0, 0] == want[0] and out_k[0, 0, 0, 1] == wneg[0], (gs, vcode, sb)
 
 
+def pin_kv_quantize(O):
+    """Contiguous quantize ("FP4 KV Cache Quantization"): block j of row i lands at codes
+    [i, 8j:8j+8] and scale [i, j], and every block whose exact-arithmetic result is clear of
+    midpoints and near-ties equals it; grid-representable rows round-trip exactly through
+    the contiguous dequantize."""
+    rng = np.random.Generator(np.random.PCG64(31))
+    recipes = [None, O.Recipe(256.0, 0, False), O.Recipe(256.0, 1, False),
+               O.Recipe(256.0, 0, True)]
+    checked = 0
+    for ri, recipe in enumerate(recipes):
+        for dt in (torch.float16, torch.bfloat16):
+            rows, cols = 5, 48
+            x = rng.standard_normal((rows, cols)).astype(np.float32)
+            x *= rng.uniform(0.05, 20.0, size=(rows, 1)).astype(np.float32)
+            x = from_bits(to_bits(x, dt), dt)
+            cap = O.e4m3_max(recipe)
+            gs = float(np.float32(np.abs(x).max() / (6 * cap)))
+            codes, sf = O.kv_quantize(to_bits(x, dt), dt == torch.bfloat16, gs, recipe)
+            assert codes.shape == (rows, cols // 2) and sf.shape == (rows, cols // 16)
+            for i in range(rows):
+                for j in range(cols // 16):
+                    xb = x[i, 16 * j:16 * j + 16]
+                    got = (int(sf[i, j]), unpack(codes[i, 8 * j:8 * j + 8]))
+                    sa, ca, Sa, clear_a = exact_candidate(xb, gs, "A", cap)
+                    if recipe is None:
+                        if clear_a:
+                            assert got == (sa, ca), (i, j, got, sa, ca)
+                            checked += 1
+                        continue
+                    sb, cb, Sb, clear_b = exact_candidate(xb, gs, "B", 448.0)
+                    if not (clear_a and clear_b):
+                        continue
+                    mse = recipe.err_mode == 1
+                    EA, EB = exact_error(xb, ca, Sa, gs, mse), exact_error(xb, cb, Sb, gs, mse)
+                    band = Fraction(1, 1 << 5) if recipe.err_use_fast_math else Fraction(1, 1 << 16)
+                    if abs(EA - EB) <= band * max(EA, EB):
+                        continue
+                    assert got == ((sb, cb) if EB < EA else (sa, ca)), (ri, i, j)
+                    checked += 1
+    assert checked >= 40, checked
+    # exact round trip of grid-representable rows (scale 2^k times an E4M3 value)
+    for dt in (torch.float16, torch.bfloat16):
+        gs = 2.0 ** -6
+        rows = []
+        for _ in range(3):
+            blocks = [_grid_block(rng, float(torch_e4m3_values()[int(rng.integers(56, 100))]),
+                                  gs, dt)[1] for _ in range(4)]
+            rows.append(np.concatenate(blocks))
+        x = np.stack(rows)
+        codes, sf = O.kv_quantize(to_bits(x, dt), dt == torch.bfloat16, gs, None)
+        back = O.kv_dequantize(codes, sf, gs, dt == torch.bfloat16)
+        assert np.array_equal(back, to_bits(x, dt))
+
+
+def pin_kv_dequantize(O):
+    """Contiguous dequantize of every (code, scale byte) pair equals
+    round_out(fp32(fp32(e2m1 * S) * gs)) from numpy binary32 arithmetic and library casts,
+    with element d of row i taking scale [i, d // 16] and nibble d % 2 of byte [i, d // 2]."""
+    rng = np.random.Generator(np.random.PCG64(32))
+    grid = np.array([float(x) for x in e2m1_grid()], np.float32)
+    code_val = np.concatenate([grid, -grid]).astype(np.float32)
+    sval = torch_e4m3_values().astype(np.float32)
+    rows, cols = 64, 64
+    codes = rng.integers(0, 256, size=(rows, cols // 2), dtype=np.uint8)
+    sf = rng.integers(0, 256, size=(rows, cols // 16), dtype=np.uint8)
+    sf[sf % 128 == 127] = 0x38  # no NaN scale bytes
+    sf[0, :] = np.arange(4, dtype=np.uint8)  # subnormal scales
+    nib = np.stack([codes & 0xF, codes >> 4], -1).reshape(rows, cols)
+    S = sval[sf].repeat(16, axis=-1)
+    for gs, out_dt in ((1.0, torch.bfloat16), (float(np.float32(0.013)), torch.float16),
+                       (float(np.float32(3.7 / 2688)), torch.bfloat16)):
+        out = O.kv_dequantize(codes, sf, gs, out_dt == torch.bfloat16)
+        want = (code_val[nib] * S).astype(np.float32) * np.float32(gs)
+        assert np.array_equal(out, to_bits(want.astype(np.float32), out_dt)), gs
+
+
 ALL_PINS = [
     pin_e2m1_decode, pin_e2m1_encode, pin_e4m3_decode, pin_e4m3_encode, pin_f16, pin_bf16,
     pin_global_scale, pin_roundtrip, pin_block_vs_exact, pin_4over6_behaviour,
     pin_recipe_mismatch, pin_append_addressing, pin_dequant, pin_materialize,
     pin_materialize_is_dequant_over_gs, pin_exact_tie_keeps_amax6,
     pin_fast_math_differs_only_near_ties, pin_dequant_multiplication_order,
+    pin_kv_quantize, pin_kv_dequantize,
 ]

@@ -68,6 +68,18 @@ MUTANTS = {
     "materialize_v_uses_k_table": (
         "int64_t col = shared ? b * max_num_pages + j : (b * 2 + kv) * max_num_pages + j;",
         "int64_t col = shared ? b * max_num_pages + j : (b * 2) * max_num_pages + j;"),
+    "kv_quantize_blocks_rotated": (
+        "quantize_block(xb, gs, r, codes + i * (cols / 2) + 8 * j, sf + i * (cols / 16) + j, NULL,",
+        "quantize_block(xb, gs, r, codes + i * (cols / 2) + 8 * ((j + 1) % (cols / 16)),\n"
+        "                     sf + i * (cols / 16) + ((j + 1) % (cols / 16)), NULL,"),
+    "kv_quantize_ignores_recipe": (
+        "quantize_block(xb, gs, r, codes + i * (cols / 2)", "quantize_block(xb, gs, NULL, codes + i * (cols / 2)"),
+    "kv_dequantize_nibble_order": (
+        "uint32_t code = (d % 2 == 0) ? (byte & 0xFu) : (byte >> 4);\n      out[i * cols + d]",
+        "uint32_t code = (d % 2 == 1) ? (byte & 0xFu) : (byte >> 4);\n      out[i * cols + d]"),
+    "kv_dequantize_scale_of_next_block": (
+        "dequant_value(code, sf[i * (cols / 16) + d / 16], gs, out_bf16);",
+        "dequant_value(code, sf[i * (cols / 16) + ((d / 16) + 1) % (cols / 16)], gs, out_bf16);"),
     "materialize_applies_nothing": (
         "double w = oracle_e2m1_decode(code) * oracle_e4m3_decode(sf[soff + d / 16]);",
         "double w = oracle_e2m1_decode(code);"),
