@@ -76,7 +76,8 @@ def op_bytes(w: W.Workload, n_active_pages: int):
 CSRC = os.path.join(ROOT, "nvfp4_paged_kv_02_gb300", "csrc")
 KERNEL_SOURCES = {
     "append": ["append.cu"], "dequant_paged": ["dequant.cu"],
-    "materialize": ["materialize.cu"],
+    "materialize": ["materialize.cu"], "kv_quantize": ["append.cu"],
+    "kv_dequantize": ["dequant.cu"],
 }
 SHARED_SOURCES = ["device.cuh", "internal.h", "pipeline.cuh", "scan.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic_large_pool.md")
@@ -220,32 +221,119 @@ class Step:
                 float(self.gv.item()), self.lay, self.recipe, self.status)
             del pk, pv
 
-    def run(self, ev=None):
-        nv, w = self.nv, self.w
-        rec = (lambda i: ev[i].record()) if ev is not None else (lambda i: None)
-        rec(0)
-        nv.nvfp4_make_global_scale(self.k, self.recipe, out=self.gk)
-        nv.nvfp4_make_global_scale(self.v, self.recipe, out=self.gv)
-        rec(1)
-        rec(2)
+        self._ops = [self._global_scales, self._append, self._dequant, self._materialize]
+
+    NAMES = ("global_scale", "append", "dequant_paged", "materialize")
+
+    def _global_scales(self):
+        self.nv.nvfp4_make_global_scale(self.k, self.recipe, out=self.gk)
+        self.nv.nvfp4_make_global_scale(self.v, self.recipe, out=self.gv)
+
+    def _append(self):
         # the scales stay on the device: no host round trip inside the step
-        nv.nvfp4_quantize_append_paged(self.k, self.v, self.bi, self.pos, self.cache, self.sf,
-                                       self.kv_indices, self.kv_indptr, self.last, self.gk,
-                                       self.gv, self.lay, self.recipe, self.status)
-        rec(3)
-        nv.nvfp4_dequantize_paged(self.cache, self.sf, self.bt, self.seq_lens, self.gk, self.gv,
-                                  self.out_k, self.out_v, self.lay, self.status)
-        rec(4)
-        nv.nvfp4_materialize_fp8(self.cache[0], self.cache[1], self.sf[0], self.sf[1],
-                                 self.mat_bt, self.seq_lens, w.max_kv_len, w.mat_shared, self.fp8,
-                                 self.indptr, w.mat_num_pages, self.lay, self.tables, True,
-                                 self.status)
-        rec(5)
+        self.nv.nvfp4_quantize_append_paged(
+            self.k, self.v, self.bi, self.pos, self.cache, self.sf, self.kv_indices,
+            self.kv_indptr, self.last, self.gk, self.gv, self.lay, self.recipe, self.status)
+
+    def _dequant(self):
+        self.nv.nvfp4_dequantize_paged(self.cache, self.sf, self.bt, self.seq_lens, self.gk,
+                                       self.gv, self.out_k, self.out_v, self.lay, self.status)
+
+    def _materialize(self):
+        w = self.w
+        self.nv.nvfp4_materialize_fp8(
+            self.cache[0], self.cache[1], self.sf[0], self.sf[1], self.mat_bt, self.seq_lens,
+            w.max_kv_len, w.mat_shared, self.fp8, self.indptr, w.mat_num_pages, self.lay,
+            self.tables, True, self.status)
+
+    def run(self, ev=None, flush=None):
+        run_ops(self._ops, ev, flush)
+
+    def op_bytes(self):
+        return op_bytes(self.w, active_pages(self.w))
+
+    def config(self):
+        w = self.w
+        return {"workload": w.name, "batch": w.B, "tokens": w.nnz, "page_size": w.ps,
+                "num_kv_heads": w.H, "head_dim": w.D,
+                "kv_layout": "NHD" if w.layout == W.NHD else "HND",
+                "input_dtype": str(w.dtype).replace("torch.", ""),
+                "recipe": None if w.recipe is None else vars(w.recipe),
+                "pool_pages": w.num_pages, "active_pages": active_pages(w)}
+
+
+def run_ops(ops, ev=None, flush=None):
+    """Run the ops in order; ev (two events per op) brackets each op; flush, when given,
+    runs before each op, outside its events."""
+    for i, op in enumerate(ops):
+        if flush is not None:
+            flush()
+        if ev is not None:
+            ev[2 * i].record()
+        op()
+        if ev is not None:
+            ev[2 * i + 1].record()
+
+
+class ContigStep:
+    """The contiguous form ("FP4 KV Cache Quantization": nvfp4_kv_quantize and
+    nvfp4_kv_dequantize) on the large-pool K and V rows, each a [tokens, H*D] tensor: the two
+    global scales, the quantize of each tensor, then the dequantize of each."""
+
+    NAMES = ("global_scale", "kv_quantize", "kv_dequantize")
+
+    def __init__(self, w: W.Workload, dev: torch.device):
+        import nvfp4_paged_kv_02_gb300 as nv
+        self.nv, self.w, self.dev = nv, w, dev
+        r = w.recipe
+        self.recipe = None if r is None else nv.NVFP44Over6Config(
+            r.e4m3_max, "MSE" if r.err_mode else "MAE", bool(r.err_use_fast_math))
+        self.rows, self.cols = w.nnz, w.H * w.D
+        self.k = w.k.to(dev).view(self.rows, self.cols)
+        self.v = w.v.to(dev).view(self.rows, self.cols)
+        u8 = dict(dtype=torch.uint8, device=dev)
+        self.q = [(torch.empty((self.rows, self.cols // 2), **u8),
+                   torch.empty((self.rows, self.cols // 16), **u8)) for _ in range(2)]
+        self.out = [torch.empty((self.rows, self.cols), dtype=w.dtype, device=dev)
+                    for _ in range(2)]
+        self.gk = torch.empty(1, dtype=torch.float32, device=dev)
+        self.gv = torch.empty(1, dtype=torch.float32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.launches_per_step = 8  # 2 x (amax + finalize), 2 quantize, 2 dequantize
+        self._ops = [self._global_scales, self._quantize, self._dequantize]
+
+    def _global_scales(self):
+        self.nv.nvfp4_make_global_scale(self.k, self.recipe, out=self.gk)
+        self.nv.nvfp4_make_global_scale(self.v, self.recipe, out=self.gv)
+
+    def _quantize(self):
+        for x, g, q in ((self.k, self.gk, self.q[0]), (self.v, self.gv, self.q[1])):
+            self.nv.nvfp4_kv_quantize(x, g, self.recipe, out=q, dev_status=self.status)
+
+    def _dequantize(self):
+        for q, g, o in ((self.q[0], self.gk, self.out[0]), (self.q[1], self.gv, self.out[1])):
+            self.nv.nvfp4_kv_dequantize(q[0], q[1], g, o.dtype, out=o)
+
+    def run(self, ev=None, flush=None):
+        run_ops(self._ops, ev, flush)
+
+    def op_bytes(self):
+        n = self.rows * self.cols
+        per = 2 * n * 2 + 2 * (n // 2 + n // 16)  # both tensors: 16-bit side + codes + scales
+        return ({"global_scale": 2 * n * 2, "kv_quantize": per, "kv_dequantize": per},
+                {"global_scale": self.rows, "kv_quantize": self.rows,
+                 "kv_dequantize": self.rows})
+
+    def config(self):
+        w = self.w
+        return {"workload": "contig", "source": "large_pool K and V rows", "tokens": self.rows,
+                "cols": self.cols, "input_dtype": str(w.dtype).replace("torch.", ""),
+                "recipe": None if w.recipe is None else vars(w.recipe)}
 
 
 def make_workload(name: str, dev: torch.device, batch: int = 256,
                   pool_gb: float = W.LARGE_POOL_BYTES / 1e9) -> W.Workload:
-    if name == "large_pool":
+    if name in ("large_pool", "contig"):
         return W.large_pool(device=str(dev), B=batch, pool_bytes=pool_gb * 1e9)
     return W.NAMED[name]()
 
@@ -284,6 +372,43 @@ def time_oracle(sub: W.Workload, nthreads: int = 0) -> float:
     return time.perf_counter() - t0
 
 
+def contig_sample(w: W.Workload, n_rows: int):
+    """The first n_rows token rows of K and V as [n, H*D] host tensors, plus the algorithmic
+    bytes of the contiguous step on them."""
+    n = max(1, min(n_rows, w.nnz))
+    k = w.k[:n].reshape(n, -1).cpu()
+    v = w.v[:n].reshape(n, -1).cpu()
+    e = k.numel()
+    return (k, v), 2 * e * 2 + 2 * (2 * (2 * e * 2 + 2 * (e // 2 + e // 16)))
+
+
+def time_oracle_contig(kv, recipe) -> float:
+    import oracle
+    t0 = time.perf_counter()
+    for x in kv:
+        bits = W.bits16(x)
+        bf16 = x.dtype == torch.bfloat16
+        gs = oracle.global_scale(bits, bf16, recipe)
+        codes, sf = oracle.kv_quantize(bits, bf16, gs, recipe)
+        oracle.kv_dequantize(codes, sf, gs, bf16)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline_contig(w: W.Workload, target_s: float = 15.0):
+    import oracle
+    n = 4096
+    kv, nbytes = contig_sample(w, n)
+    dt = time_oracle_contig(kv, w.recipe)
+    while dt < target_s / 4 and n < w.nnz:
+        n = min(w.nnz, max(n + 1, int(n * min(8.0, target_s / 2 / max(dt, 1e-3)))))
+        kv, nbytes = contig_sample(w, n)
+        dt = time_oracle_contig(kv, w.recipe)
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"first {n} of {w.nnz} K and V rows of the contig workload, whole step, "
+                      f"{dt:.1f} s"}
+
+
 def cpu_baseline(w: W.Workload, target_s: float = 15.0):
     import oracle
     cores = oracle.max_threads()
@@ -303,22 +428,30 @@ def reference_arm(args, w: W.Workload):
     """The CPU oracle as the reference implementation: K timed steps (after W untimed) on a
     bounded sample of the same workload."""
     import oracle
-    n_req = max(1, min(w.B, args.ref_requests))
-    sub, nbytes = oracle_sample(w, n_req)
+    if args.workload == "contig":
+        n_rows = 8192 * max(1, args.ref_requests)
+        kv, nbytes = contig_sample(w, n_rows)
+        timer = lambda: time_oracle_contig(kv, w.recipe)
+        sample = f"first {kv[0].shape[0]} of {w.nnz} K and V rows"
+        sample_cfg = {"workload": "contig", "sample_rows": kv[0].shape[0]}
+    else:
+        n_req = max(1, min(w.B, args.ref_requests))
+        sub, nbytes = oracle_sample(w, n_req)
+        timer = lambda: time_oracle(sub)
+        sample = f"first {n_req} of {w.B} requests ({sub.nnz} tokens)"
+        sample_cfg = {"workload": w.name, "sample_requests": n_req, "sample_tokens": sub.nnz}
     for _ in range(args.warmup):
-        time_oracle(sub)
-    times = [time_oracle(sub) for _ in range(args.steps)]
+        timer()
+    times = [timer() for _ in range(args.steps)]
     dt = sum(times) / len(times)
     v = nbytes / dt / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": {"workload": w.name, "sample_requests": n_req,
-                                            "sample_tokens": sub.nnz},
+            "data": "synthetic", "config": sample_cfg,
             "cpu_baseline": {"value": v, "unit": "GB/s", "cores": oracle.max_threads(),
                              "kind": "oracle",
-                             "sample": f"first {n_req} of {w.B} requests ({sub.nnz} tokens), "
-                                       f"whole step per timed step"},
+                             "sample": f"{sample}, whole step per timed step"},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -331,7 +464,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="large_pool",
-                    choices=["large_pool", "decode", "prefill", "materialize", "tiny"])
+                    choices=["large_pool", "decode", "prefill", "materialize", "tiny", "contig"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--ref-requests", type=int, default=4)
     ap.add_argument("--batch", type=int, default=256, help="large_pool: requests")
@@ -365,11 +498,16 @@ def main():
     import nvfp4_paged_kv_02_gb300 as nv
     nv.load()
     w = make_workload(args.workload, dev, args.batch, args.pool_gb)
-    step = Step(w, dev)
-    nbytes, ntok = op_bytes(w, active_pages(w))
+    step = ContigStep(w, dev) if args.workload == "contig" else Step(w, dev)
+    nbytes, ntok = step.op_bytes()
+    n_ops = len(step.NAMES)
     total_bytes = sum(nbytes.values())
-    small = total_bytes < 4 * 129e6
+    small = max(nbytes.values()) < 1e9
+    # L2 flush before every op of workloads whose ops are under 1 GB (so no op reads what the
+    # one before it left in L2): write 256 MB, then read another 256 MB, so that the flush's
+    # own dirty lines are written back before the op starts instead of competing with it
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if small else None
+    flush_read = torch.zeros(256 << 20, dtype=torch.uint8, device=dev) if small else None
 
     for _ in range(args.warmup):
         step.run()
@@ -377,7 +515,16 @@ def main():
     if int(step.status.item()) != 0:
         raise SystemExit(f"device status {int(step.status.item()):#x} after warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * n_ops)]
+           for _ in range(args.steps)]
+
+    flushes = [0]
+
+    def flush_l2():
+        flushes[0] += 1
+        flush.fill_(flushes[0] & 0xFF)
+        flush_read.sum()
+
     os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
     clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv"))
     if world > 1:
@@ -389,14 +536,16 @@ def main():
     step_ms = []
     h0 = time.time()
     for s in range(args.steps):
-        if flush is not None:
-            flush.fill_(s & 0xFF)
-        step.run(evs[s])
+        step.run(evs[s], flush_l2 if flush is not None else None)
     torch.cuda.synchronize(dev)
     h1 = time.time()
     clk = clocks.stop(h0, h1)
     for s in range(args.steps):
-        step_ms.append(evs[s][0].elapsed_time(evs[s][5]))
+        if flush is None:
+            step_ms.append(evs[s][0].elapsed_time(evs[s][2 * n_ops - 1]))
+        else:  # the device time of the ops, without the flushes between them
+            step_ms.append(sum(evs[s][2 * i].elapsed_time(evs[s][2 * i + 1])
+                               for i in range(n_ops)))
     ms = float(np.mean(step_ms))
     if world > 1:
         import torch.distributed as dist
@@ -405,7 +554,7 @@ def main():
         ms = float(tt.item())
         dist.barrier()
     # per-op device time (mean over steps)
-    seg = {"global_scale": (0, 1), "append": (2, 3), "dequant_paged": (3, 4), "materialize": (4, 5)}
+    seg = {k: (2 * i, 2 * i + 1) for i, k in enumerate(step.NAMES)}
     op_ms = {k: float(np.mean([evs[s][a].elapsed_time(evs[s][b]) for s in range(args.steps)]))
              for k, (a, b) in seg.items()}
     peak, peak_kind = measured_peaks()
@@ -416,7 +565,7 @@ def main():
                   "pct_of_8TBs": 100 * gbs / NOMINAL_HBM_GBS,
                   "pct_of_measured_copy": 100 * gbs / peak,
                   "tokens_per_s": ntok[k] / (op_ms[k] * 1e-3)}
-    dom = max(("append", "dequant_paged", "materialize"), key=lambda k: op_ms[k])
+    dom = max(step.NAMES[1:], key=lambda k: op_ms[k])
     value = world * total_bytes / (ms * 1e-3) / 1e9
     status = int(step.status.item())
 
@@ -425,7 +574,7 @@ def main():
         e2e = measure_e2e(step, w, args, total_bytes, world)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w)
+        cpu = cpu_baseline(w) if isinstance(step, Step) else cpu_baseline_contig(w)
 
     if rank == 0:
         line = {
@@ -433,13 +582,9 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": w.name, "batch": w.B, "tokens": w.nnz, "page_size": w.ps,
-                       "num_kv_heads": w.H, "head_dim": w.D,
-                       "kv_layout": "NHD" if w.layout == W.NHD else "HND",
-                       "input_dtype": str(w.dtype).replace("torch.", ""),
-                       "recipe": None if w.recipe is None else vars(w.recipe),
-                       "pool_pages": w.num_pages, "active_pages": active_pages(w),
-                       "l2": "flushed with a 256 MB write between steps" if small
+            "config": {**step.config(),
+                       "l2": "flushed before every op (256 MB write, then 256 MB read), "
+                             "outside the timed ops" if small
                        else "inputs larger than L2 (129 MB); no flush",
                        "parallelism": f"replicas x{world}"},
             "ops": ops,

@@ -13,6 +13,9 @@
  *   - the per-tensor global decode scale and the recipe's block-scale clamp
  *       ("flashinfer.quantization" index: "NVFP4 4over6 Recipes", make_nvfp4_global_scale,
  *        nvfp4_e4m3_max)
+ *   - contiguous quantize / dequantize with the same block rule
+ *       ("flashinfer.quantization" index: "FP4 KV Cache Quantization", nvfp4_kv_quantize,
+ *        nvfp4_kv_dequantize)
  *
  * Number formats: E2M1 codes (grid {0,0.5,1,1.5,2,3,4,6}, 4 bits, two per byte, element
  * 2k in the low nibble); E4M3 (e4m3fn) block scales stored as bytes, one per 16
@@ -247,6 +250,39 @@ nvfp4_status nvfp4_materialize_fp8(
     int32_t batch_size, int32_t max_kv_len, const int32_t* kv_page_indptr, int64_t num_pages,
     uint8_t* out, int64_t out_num_pages, int32_t* fp8_block_tables,
     int32_t zero_fp8_block_tables, int32_t* dev_status, void* stream);
+
+/* Quantize a contiguous fp16/bf16 tensor to NVFP4 with linear block scales
+ * ("flashinfer.quantization" index, "FP4 KV Cache Quantization": nvfp4_kv_quantize).
+ * The tensor is `rows` rows of `cols` elements (all leading dimensions flattened); row i
+ * starts `row_stride` elements after row i-1. Every 16-element block gets the rule of
+ * nvfp4_quantize_append_paged (standard NVFP4, or 4over6 with `recipe`):
+ *   input        device, 16-byte aligned, row_stride a multiple of 8 elements, >= cols.
+ *   dtype        NVFP4_F16 or NVFP4_BF16.
+ *   global_scale device float: the global decode scale (for example from
+ *                nvfp4_make_global_scale with the same recipe). Not positive finite:
+ *                NVFP4_DEV_BAD_SCALE is reported and nothing is written.
+ *   fp4_out      device uint8 [rows, cols/2], contiguous, 8-byte aligned: element 2k of a
+ *                row in the low nibble of byte k.
+ *   sf_out       device uint8 [rows, cols/16], contiguous: the E4M3 scale of block j.
+ * Requirements: cols % 16 == 0, cols > 0, rows >= 0. */
+nvfp4_status nvfp4_kv_quantize(const void* input, int32_t dtype, int64_t rows, int32_t cols,
+                               int64_t row_stride, const float* global_scale,
+                               const nvfp4_4over6_config* recipe, uint8_t* fp4_out,
+                               uint8_t* sf_out, int32_t* dev_status, void* stream);
+
+/* Dequantize a contiguous NVFP4 tensor with linear block scales
+ * ("flashinfer.quantization" index, "FP4 KV Cache Quantization": nvfp4_kv_dequantize):
+ *   out[i, d] = round_out( (e2m1(q[i, d]) * S[i, d/16]) * gs )
+ * with the same rounding as nvfp4_dequantize_paged.
+ *   fp4          device uint8 [rows, cols/2], contiguous, 8-byte aligned.
+ *   sf           device uint8 [rows, cols/16], contiguous.
+ *   global_scale device float.
+ *   out          device [rows, cols] of out_dtype (NVFP4_F16 or NVFP4_BF16), contiguous,
+ *                16-byte aligned.
+ * Requirements: cols % 16 == 0, cols > 0, rows >= 0. */
+nvfp4_status nvfp4_kv_dequantize(const uint8_t* fp4, const uint8_t* sf, int64_t rows,
+                                 int32_t cols, const float* global_scale, void* out,
+                                 int32_t out_dtype, int32_t* dev_status, void* stream);
 
 #ifdef __cplusplus
 }

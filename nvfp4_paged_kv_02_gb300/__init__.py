@@ -30,7 +30,7 @@ __all__ = [
     "NVFP44Over6Config", "NVFP4KVError", "PagedCache", "load", "nvfp4_e4m3_max",
     "nvfp4_make_global_scale", "nvfp4_quantize_append_paged", "nvfp4_dequantize_paged",
     "nvfp4_materialize_fp8", "nvfp4_materialize_fp8_out_pages", "NVFP4KVMaterializer",
-    "paged_caches", "LIB_PATH",
+    "paged_caches", "LIB_PATH", "nvfp4_kv_quantize", "nvfp4_kv_dequantize",
 ]
 
 LIB_PATH = _build.LIB_PATH
@@ -110,6 +110,10 @@ def load() -> ctypes.CDLL:
         L.nvfp4_materialize_fp8.argtypes = [
             _Cache, _Cache, i32, i32, i32, i32, vp, i32, i32, vp, i32, i32, vp, i64, vp, i64, vp,
             i32, vp, vp]
+        L.nvfp4_kv_quantize.restype = i32
+        L.nvfp4_kv_quantize.argtypes = [vp, i32, i64, i32, i64, vp, vp, vp, vp, vp, vp]
+        L.nvfp4_kv_dequantize.restype = i32
+        L.nvfp4_kv_dequantize.argtypes = [vp, vp, i64, i32, vp, vp, i32, vp, vp]
         _lib = L
         return L
 
@@ -382,3 +386,66 @@ class NVFP4KVMaterializer:
             _ptr(kv_page_indptr), out.shape[0] - 1, _ptr(out), out.shape[0],
             _ptr(fp8_block_tables), 0, _ptr(dev_status), _stream(self.device)))
         return out, fp8_block_tables
+
+
+def _scale_tensor(global_scale, device: torch.device) -> torch.Tensor:
+    if isinstance(global_scale, torch.Tensor):
+        if global_scale.dtype != torch.float32 or global_scale.numel() < 1:
+            raise ValueError("global_scale must be a float32 CUDA tensor")
+        return global_scale
+    return torch.tensor([float(global_scale)], dtype=torch.float32, device=device)
+
+
+def nvfp4_kv_quantize(input: torch.Tensor, global_scale,
+                      nvfp4_4over6: Optional[NVFP44Over6Config] = None,
+                      out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None,
+                      dev_status: Optional[torch.Tensor] = None):
+    """Quantize a fp16/bf16 tensor [..., D] (D % 16 == 0) to NVFP4 with linear block scales.
+    Returns (fp4_data uint8 [..., D/2], block_scales uint8 [..., D/16]); `global_scale` is
+    the decode scale (a 1-element float32 CUDA tensor, or a float)."""
+    if input.dim() < 1 or input.stride(-1) != 1:
+        raise ValueError("input must have a contiguous last dimension")
+    cols = input.shape[-1]
+    lead = input.shape[:-1]
+    x2 = input.reshape(-1, cols) if input.numel() else input.view(0, cols)
+    if x2.stride(-1) != 1:
+        raise ValueError("input rows must be contiguous")
+    rows = x2.shape[0]
+    if out is None:
+        fp4 = torch.empty((*lead, cols // 2), dtype=torch.uint8, device=input.device)
+        sf = torch.empty((*lead, cols // 16), dtype=torch.uint8, device=input.device)
+    else:
+        fp4, sf = out
+        if fp4.shape != (*lead, cols // 2) or sf.shape != (*lead, cols // 16) \
+                or not fp4.is_contiguous() or not sf.is_contiguous():
+            raise ValueError("out must be contiguous ([..., D/2], [..., D/16]) uint8 tensors")
+    gs = _scale_tensor(global_scale, input.device)
+    _check("nvfp4_kv_quantize", load().nvfp4_kv_quantize(
+        _ptr(x2), _dtype_code(input.dtype), rows, cols, x2.stride(0) if rows > 1 else cols,
+        _ptr(gs), _recipe(nvfp4_4over6), _ptr(fp4), _ptr(sf), _ptr(dev_status),
+        _stream(input.device)))
+    return fp4, sf
+
+
+def nvfp4_kv_dequantize(fp4_data: torch.Tensor, block_scales: torch.Tensor, global_scale,
+                        output_dtype: torch.dtype = torch.bfloat16,
+                        out: Optional[torch.Tensor] = None,
+                        dev_status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Dequantize NVFP4 codes [..., D/2] with linear block scales [..., D/16] to
+    output_dtype [..., D]: e2m1 * block_scale * global_scale."""
+    if not fp4_data.is_contiguous() or not block_scales.is_contiguous():
+        raise ValueError("fp4_data and block_scales must be contiguous")
+    cols = 2 * fp4_data.shape[-1]
+    lead = fp4_data.shape[:-1]
+    if block_scales.shape != (*lead, cols // 16):
+        raise ValueError("block_scales must be [..., D/16]")
+    rows = fp4_data.numel() // fp4_data.shape[-1] if fp4_data.shape[-1] else 0
+    if out is None:
+        out = torch.empty((*lead, cols), dtype=output_dtype, device=fp4_data.device)
+    elif out.shape != (*lead, cols) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [..., D] tensor")
+    gs = _scale_tensor(global_scale, fp4_data.device)
+    _check("nvfp4_kv_dequantize", load().nvfp4_kv_dequantize(
+        _ptr(fp4_data), _ptr(block_scales), rows, cols, _ptr(gs), _ptr(out),
+        _dtype_code(out.dtype), _ptr(dev_status), _stream(fp4_data.device)))
+    return out

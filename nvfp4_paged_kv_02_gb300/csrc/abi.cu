@@ -274,6 +274,82 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_append_paged_dev_scale(
                      1.0f, k_scale, v_scale, recipe, dev_status, stream);
 }
 
+NVFP4_EXPORT nvfp4_status nvfp4_kv_quantize(const void* input, int32_t dtype, int64_t rows,
+                                            int32_t cols, int64_t row_stride,
+                                            const float* global_scale,
+                                            const nvfp4_4over6_config* recipe,
+                                            uint8_t* fp4_out, uint8_t* sf_out,
+                                            int32_t* dev_status, void* stream) {
+  clear_error();
+  const char* fn = "nvfp4_kv_quantize";
+  if (nvfp4_status st = check_recipe(recipe)) return st;
+  if (dtype != NVFP4_F16 && dtype != NVFP4_BF16)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_kv_quantize: dtype must be NVFP4_F16 or NVFP4_BF16");
+  if (cols <= 0 || cols % 16 != 0)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_kv_quantize: cols must be a positive multiple of 16");
+  if (rows < 0) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_kv_quantize: rows must be >= 0");
+  if (rows == 0) return NVFP4_OK;
+  if (row_stride < cols)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_kv_quantize: row_stride must be >= cols");
+  if (!input || !global_scale || !fp4_out || !sf_out)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_kv_quantize: null device pointer");
+  if (!aligned(input, 16) || row_stride % 8 != 0 || !aligned(fp4_out, 8) || !aligned(global_scale, 4))
+    return fail(NVFP4_ERR_ALIGNMENT, std::string(fn) + ": input must be 16-byte aligned with a row stride a multiple of 8 elements, fp4_out 8-byte aligned");
+  AppendArgs a{};
+  a.k = static_cast<const uint8_t*>(input);
+  a.v = nullptr;
+  a.k_row_bytes = row_stride * 2;
+  a.nnz = rows;
+  a.H = 1;
+  a.D = cols;
+  a.nb = cols / 16;
+  a.div_nb = make_div(a.nb);
+  a.div_H = make_div(1);
+  a.div_ps = make_div(1);
+  a.div_row_blocks = make_div(a.nb);
+  a.kc = nvfp4_paged_cache{fp4_out, sf_out, cols / 2, cols / 16, rows};
+  a.ps = 1;
+  a.layout = NVFP4_NHD;
+  a.gs[0] = a.gs[1] = 1.0f;
+  a.gs_dev[0] = a.gs_dev[1] = global_scale;
+  a.cap_a = nvfp4_e4m3_max(recipe);
+  a.neg_zero = 0x80000000u;
+  a.pipe = pipe_test_from_env();
+  a.status = dev_status;
+  a.contig = 1;
+  int mode = 0;
+  if (recipe) mode = 1 + (recipe->err_mode == NVFP4_ERR_MSE ? 1 : 0) + (recipe->err_use_fast_math ? 2 : 0);
+  const bool vec256 = aligned(input, 32) && row_stride % 16 == 0;
+  return launch_append(a, dtype == NVFP4_BF16, mode, vec256, static_cast<cudaStream_t>(stream));
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_kv_dequantize(const uint8_t* fp4, const uint8_t* sf,
+                                              int64_t rows, int32_t cols,
+                                              const float* global_scale, void* out,
+                                              int32_t out_dtype, int32_t* dev_status,
+                                              void* stream) {
+  clear_error();
+  (void)dev_status;  // no device-held indices: nothing to report
+  if (out_dtype != NVFP4_F16 && out_dtype != NVFP4_BF16)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_kv_dequantize: out_dtype must be NVFP4_F16 or NVFP4_BF16");
+  if (cols <= 0 || cols % 16 != 0)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_kv_dequantize: cols must be a positive multiple of 16");
+  if (rows < 0) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_kv_dequantize: rows must be >= 0");
+  if (rows == 0) return NVFP4_OK;
+  if (!fp4 || !sf || !global_scale || !out)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_kv_dequantize: null device pointer");
+  if (!aligned(fp4, 8) || !aligned(out, 16) || !aligned(global_scale, 4))
+    return fail(NVFP4_ERR_ALIGNMENT, "nvfp4_kv_dequantize: fp4 must be 8-byte aligned and out 16-byte aligned");
+  KvDequantArgs a{};
+  a.codes = fp4;
+  a.sf = sf;
+  a.blocks = rows * (cols / 16);
+  a.gs = global_scale;
+  a.out = static_cast<uint8_t*>(out);
+  return launch_kv_dequant(a, out_dtype == NVFP4_BF16, aligned(out, 32),
+                           static_cast<cudaStream_t>(stream));
+}
+
 NVFP4_EXPORT nvfp4_status nvfp4_dequantize_paged(
     nvfp4_paged_cache k_cache, nvfp4_paged_cache v_cache, int32_t page_size,
     int32_t num_kv_heads, int32_t head_dim, int32_t kv_layout, const void* block_tables,

@@ -355,30 +355,35 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
     const uint8_t* pk = a.k + i * a.k_row_bytes + col;
     const uint8_t* pv = a.v + i * a.v_row_bytes + col;
     const U32x8 xk = VEC256 ? ld_nc_256(pk) : ld_nc_2x128(pk);
-    const U32x8 xv = VEC256 ? ld_nc_256(pv) : ld_nc_2x128(pv);
+    U32x8 xv{};
+    if (a.v != nullptr) xv = VEC256 ? ld_nc_256(pv) : ld_nc_2x128(pv);
 
-    const int32_t b = __ldg(a.batch_indices + i);
-    const int32_t pos = __ldg(a.positions + i);
-    if (b < 0 || b >= a.batch_size) {
-      flag(a.status, NVFP4_DEV_BAD_BATCH);
-      continue;
+    int64_t page = i, slot = 0;  // contiguous form: row i is "page" i (stride H*D/2)
+    if (!a.contig) {
+      const int32_t b = __ldg(a.batch_indices + i);
+      const int32_t pos = __ldg(a.positions + i);
+      if (b < 0 || b >= a.batch_size) {
+        flag(a.status, NVFP4_DEV_BAD_BATCH);
+        continue;
+      }
+      const int64_t start = __ldg(a.kv_indptr + b);
+      const int64_t npages = static_cast<int64_t>(__ldg(a.kv_indptr + b + 1)) - start;
+      const int64_t lp = pos >= 0 ? div_q(pos, a.div_ps) : -1;
+      bool ok = pos >= 0 && lp < npages && start >= 0 && start + lp < a.num_kv_indices;
+      if (ok && a.kv_last_page_len)
+        ok = pos < (npages - 1) * a.ps + __ldg(a.kv_last_page_len + b);
+      if (!ok) {
+        flag(a.status, NVFP4_DEV_BAD_POSITION);
+        continue;
+      }
+      page = __ldg(a.kv_indices + start + lp);
+      slot = pos - lp * a.ps;
     }
-    const int64_t start = __ldg(a.kv_indptr + b);
-    const int64_t npages = static_cast<int64_t>(__ldg(a.kv_indptr + b + 1)) - start;
-    const int64_t lp = pos >= 0 ? div_q(pos, a.div_ps) : -1;
-    bool ok = pos >= 0 && lp < npages && start >= 0 && start + lp < a.num_kv_indices;
-    if (ok && a.kv_last_page_len)
-      ok = pos < (npages - 1) * a.ps + __ldg(a.kv_last_page_len + b);
-    if (!ok) {
-      flag(a.status, NVFP4_DEV_BAD_POSITION);
-      continue;
-    }
-    const int64_t page = __ldg(a.kv_indices + start + lp);
-    const int64_t slot = pos - lp * a.ps;
     const int64_t r = a.layout == NVFP4_NHD ? slot * a.H + h : static_cast<int64_t>(h) * a.ps + slot;
 
 #pragma unroll
     for (int kv = 0; kv < 2; ++kv) {
+      if (kv == 1 && a.v == nullptr) continue;
       const nvfp4_paged_cache& c = kv ? a.vc : a.kc;
       if (page < 0 || page >= c.num_pages) {
         flag(a.status, NVFP4_DEV_BAD_PAGE);
@@ -414,9 +419,14 @@ struct RowDst {
 
 __device__ __forceinline__ RowDst resolve_row_dst(const AppendArgs& a, int64_t i) {
   RowDst d{nullptr, nullptr, nullptr, nullptr};
-  const RowMeta m = resolve_row(a, i);
   const int64_t rd = a.layout == NVFP4_NHD ? static_cast<int64_t>(a.H) * (a.D / 2) : a.D / 2;
   const int64_t rs = a.layout == NVFP4_NHD ? static_cast<int64_t>(a.H) * a.nb : a.nb;
+  if (a.contig) {
+    d.kd = a.kc.data + i * rd;
+    d.ks = a.kc.sf + i * rs;
+    return d;
+  }
+  const RowMeta m = resolve_row(a, i);
   if (m.flags & 1) {
     d.kd = a.kc.data + m.page * a.kc.data_page_stride + m.slot * rd;
     d.ks = a.kc.sf + m.page * a.kc.sf_page_stride + m.slot * rs;
@@ -431,16 +441,18 @@ __device__ __forceinline__ RowDst resolve_row_dst(const AppendArgs& a, int64_t i
 struct AppendTmaLayout {
   uint32_t rows;        // tokens per tile
   uint32_t row_bytes;   // H * D * 2 (one row of one tensor)
-  uint32_t stage_bytes; // K tile + V tile + row destinations
+  uint32_t nkv;         // tensors per stage: 2 (K and V), 1 for the contiguous form
+  uint32_t stage_bytes; // K tile [+ V tile] + row destinations
   uint32_t tables_off, stages_off, bars_off, misc_off, total;
   int ns;
 };
 
-inline AppendTmaLayout append_tma_layout(uint32_t rows, uint32_t row_bytes, int ns) {
+inline AppendTmaLayout append_tma_layout(uint32_t rows, uint32_t row_bytes, uint32_t nkv, int ns) {
   AppendTmaLayout L;
   L.rows = rows;
   L.row_bytes = row_bytes;
-  L.stage_bytes = round_up(2u * rows * row_bytes + rows * sizeof(RowDst), 128);
+  L.nkv = nkv;
+  L.stage_bytes = round_up(nkv * rows * row_bytes + rows * sizeof(RowDst), 128);
   L.ns = ns;
   L.tables_off = 0;
   L.stages_off = round_up(sizeof(Tables), 128);
@@ -477,7 +489,8 @@ __global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const Append
 
   const int64_t tiles = (a.nnz + L.rows - 1) / L.rows;
   const uint32_t tile_bytes = L.rows * L.row_bytes;
-  const bool contiguous = a.k_row_bytes == L.row_bytes && a.v_row_bytes == L.row_bytes;
+  const bool contiguous =
+      a.k_row_bytes == L.row_bytes && (L.nkv == 1 || a.v_row_bytes == L.row_bytes);
   if (warp == kConsumerWarps) {
     int s = 0;
     uint32_t phase = 0, round = 0;  // phase = parity of `round`, the stage's fill count
@@ -502,21 +515,23 @@ __global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const Append
         break;
       }
       uint8_t* st = stages + static_cast<uint32_t>(s) * L.stage_bytes;
-      RowDst* dst = reinterpret_cast<RowDst*>(st + 2u * tile_bytes);
+      RowDst* dst = reinterpret_cast<RowDst*>(st + L.nkv * tile_bytes);
       if (static_cast<uint32_t>(lane) < nrows) dst[lane] = d;
       __syncwarp();
-      if (lane == 0 && !withhold) mbar_arrive_expect_tx(full + s, 2u * nrows * L.row_bytes);
+      if (lane == 0 && !withhold) mbar_arrive_expect_tx(full + s, L.nkv * nrows * L.row_bytes);
       __syncwarp();
       if (contiguous) {
         if (lane == 0 && nrows > 0) {
           bulk_g2s(st, a.k + row0 * a.k_row_bytes, nrows * L.row_bytes, full + s);
-          bulk_g2s(st + tile_bytes, a.v + row0 * a.v_row_bytes, nrows * L.row_bytes, full + s);
+          if (L.nkv == 2)
+            bulk_g2s(st + tile_bytes, a.v + row0 * a.v_row_bytes, nrows * L.row_bytes, full + s);
         }
       } else if (static_cast<uint32_t>(lane) < nrows) {
         const uint32_t r = lane;
         bulk_g2s(st + r * L.row_bytes, a.k + (row0 + r) * a.k_row_bytes, L.row_bytes, full + s);
-        bulk_g2s(st + tile_bytes + r * L.row_bytes, a.v + (row0 + r) * a.v_row_bytes,
-                 L.row_bytes, full + s);
+        if (L.nkv == 2)
+          bulk_g2s(st + tile_bytes + r * L.row_bytes, a.v + (row0 + r) * a.v_row_bytes,
+                   L.row_bytes, full + s);
       }
       if (lane == 0 && !withhold) s_issued[s] = round + 1;
       __syncwarp();
@@ -551,7 +566,7 @@ __global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const Append
         break;
       }
       const uint8_t* st = stages + static_cast<uint32_t>(s) * L.stage_bytes;
-      const RowDst* dst = reinterpret_cast<const RowDst*>(st + 2u * tile_bytes);
+      const RowDst* dst = reinterpret_cast<const RowDst*>(st + L.nkv * tile_bytes);
       const int32_t nrows =
           static_cast<int32_t>(min(static_cast<int64_t>(L.rows), a.nnz - tile * L.rows));
       const int32_t nblk = nrows * row_blocks;
@@ -609,14 +624,15 @@ nvfp4_status launch_t(const AppendArgs& a, cudaStream_t stream) {
 // TMA path: tiles of up to 32 rows (the producer gives each row one lane) and about 16 KB
 // per tensor, 2 to 6 stages in 70 KB (three CTAs per SM).
 template <bool BF16, int MODE>
-nvfp4_status launch_tma(const AppendArgs& a, uint32_t row_bytes, cudaStream_t stream) {
+nvfp4_status launch_tma(const AppendArgs& a, uint32_t row_bytes, uint32_t nkv,
+                        cudaStream_t stream) {
   const auto kern = append_tma_kernel<BF16, MODE>;
-  uint32_t rows = 16384u / row_bytes;
+  uint32_t rows = (nkv == 2 ? 16384u : 32768u) / row_bytes;
   rows = rows < 1 ? 1 : (rows > 32 ? 32 : rows);
-  const uint32_t one = round_up(2u * rows * row_bytes + rows * sizeof(RowDst), 128);
+  const uint32_t one = round_up(nkv * rows * row_bytes + rows * sizeof(RowDst), 128);
   int ns = static_cast<int>((70u * 1024u) / one);
   ns = ns < 2 ? 2 : (ns > 6 ? 6 : ns);
-  const AppendTmaLayout L = append_tma_layout(rows, row_bytes, ns);
+  const AppendTmaLayout L = append_tma_layout(rows, row_bytes, nkv, ns);
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(L.total));
   const int64_t tiles = (a.nnz + rows - 1) / rows;
@@ -633,7 +649,9 @@ nvfp4_status launch_v(const AppendArgs& a, bool vec256, cudaStream_t s) {
   // one row of K and V (all heads) must fit a stage; bases and row strides are 16-byte
   // aligned by the entry point's checks
   const int64_t row_bytes = static_cast<int64_t>(a.H) * a.D * 2;
-  if (2 * row_bytes <= 48 * 1024) return launch_tma<BF16, MODE>(a, static_cast<uint32_t>(row_bytes), s);
+  const uint32_t nkv = a.v != nullptr ? 2u : 1u;
+  if (nkv * row_bytes <= 48 * 1024)
+    return launch_tma<BF16, MODE>(a, static_cast<uint32_t>(row_bytes), nkv, s);
   return vec256 ? launch_t<BF16, MODE, true>(a, s) : launch_t<BF16, MODE, false>(a, s);
 }
 

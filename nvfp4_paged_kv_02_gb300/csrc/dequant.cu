@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const DequantArgs a) 
 // decoding.
 
 template <bool OUT_BF16, bool BT64>
-__global__ void __launch_bounds__(kTmaThreads, 2) dequant_tma_kernel(const DequantArgs a,
+__global__ void __launch_bounds__(kTmaThreads, 3) dequant_tma_kernel(const DequantArgs a,
                                                                   const TmaLayout L) {
   extern __shared__ __align__(128) uint8_t smem[];
   int32_t* s_cum = reinterpret_cast<int32_t*>(smem);
@@ -279,6 +279,60 @@ __global__ void __launch_bounds__(kTmaThreads, 2) dequant_tma_kernel(const Dequa
   }
 }
 
+// ---- contiguous form ----------------------------------------------------------------
+//
+// FlashInfer "flashinfer.quantization" index, "FP4 KV Cache Quantization":
+// nvfp4_kv_dequantize on a contiguous code tensor with linear block scales. A grid-stride
+// loop over 16-element blocks; each thread loads four blocks (8 code bytes + 1 scale byte
+// each, a warp's loads being contiguous runs) before it decodes them into 32-byte stores.
+constexpr int kKvThreads = 256;
+
+template <bool OUT_BF16, bool VEC256>
+__global__ void __launch_bounds__(kKvThreads) kv_dequant_kernel(const KvDequantArgs a) {
+  const float gs = __ldg(a.gs);
+  const int64_t T = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const uint2* codes = reinterpret_cast<const uint2*>(a.codes);
+  for (int64_t b0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; b0 < a.blocks;
+       b0 += 4 * T) {
+    uint2 c[4];
+    uint32_t sc[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t b = b0 + u * T;
+      if (b < a.blocks) {
+        c[u] = __ldg(codes + b);
+        sc[u] = __ldg(a.sf + b);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t b = b0 + u * T;
+      if (b < a.blocks) {
+        const U32x8 o = decode_block<OUT_BF16>(c[u], sc[u], gs);
+        uint8_t* dst = a.out + b * 32;
+        if (VEC256) {
+          st_256(dst, o);
+        } else {
+          reinterpret_cast<uint4*>(dst)[0] = make_uint4(o.w[0], o.w[1], o.w[2], o.w[3]);
+          reinterpret_cast<uint4*>(dst)[1] = make_uint4(o.w[4], o.w[5], o.w[6], o.w[7]);
+        }
+      }
+    }
+  }
+}
+
+template <bool OUT_BF16, bool VEC256>
+nvfp4_status launch_kv(const KvDequantArgs& a, cudaStream_t stream) {
+  const auto kern = kv_dequant_kernel<OUT_BF16, VEC256>;
+  const int64_t need = (a.blocks + 4 * kKvThreads - 1) / (4 * kKvThreads);
+  const int64_t cap = static_cast<int64_t>(sm_count()) *
+                      blocks_per_sm(reinterpret_cast<const void*>(kern), kKvThreads, 0);
+  const int grid = static_cast<int>(need < cap ? need : cap);
+  if (grid <= 0) return NVFP4_OK;
+  kern<<<grid, kKvThreads, 0, stream>>>(a);
+  return check_launch("nvfp4_kv_dequantize");
+}
+
 template <bool OUT_BF16, bool BT64, bool VEC256>
 nvfp4_status launch_t(const DequantArgs& a, cudaStream_t stream) {
   const auto kern = dequant_kernel<OUT_BF16, BT64, VEC256>;
@@ -322,6 +376,12 @@ nvfp4_status launch_v(const DequantArgs& a, bool vec256, cudaStream_t s) {
 }
 
 }  // namespace
+
+nvfp4_status launch_kv_dequant(const KvDequantArgs& a, bool out_bf16, bool vec256,
+                               cudaStream_t stream) {
+  if (out_bf16) return vec256 ? launch_kv<true, true>(a, stream) : launch_kv<true, false>(a, stream);
+  return vec256 ? launch_kv<false, true>(a, stream) : launch_kv<false, false>(a, stream);
+}
 
 nvfp4_status launch_dequant(const DequantArgs& a, bool out_bf16, bool bt64, bool vec256,
                             cudaStream_t stream) {

@@ -58,6 +58,9 @@ struct AppendArgs {
   uint32_t neg_zero;  // 0x80000000 (-0.0f), passed at run time for fsq2_rn / hsq2_rn
   PipeTest pipe;
   int32_t* status;
+  // Contiguous form (nvfp4_kv_quantize): row i goes to kc.data + i * H*D/2 and
+  // kc.sf + i * H*D/16; no index arrays are read, and v is null.
+  int32_t contig;
 };
 // mode: 0 standard NVFP4; 1/2 4over6 binary32 MAE/MSE; 3/4 4over6 binary16 MAE/MSE.
 nvfp4_status launch_append(const AppendArgs& a, bool bf16, int mode, bool vec256,
@@ -80,6 +83,18 @@ struct DequantArgs {
   PipeTest pipe;
   int32_t* status;
 };
+// Contiguous dequantize (nvfp4_kv_dequantize): block k of the flattened [rows, cols] codes
+// (8 bytes at codes + 8k, scale byte sf[k]) becomes 16 outputs at out + 32k bytes.
+struct KvDequantArgs {
+  const uint8_t* codes;
+  const uint8_t* sf;
+  int64_t blocks;  // rows * cols / 16
+  const float* gs;
+  uint8_t* out;
+};
+nvfp4_status launch_kv_dequant(const KvDequantArgs& a, bool out_bf16, bool vec256,
+                               cudaStream_t stream);
+
 nvfp4_status launch_dequant(const DequantArgs& a, bool out_bf16, bool bt64, bool vec256,
                             cudaStream_t stream);
 

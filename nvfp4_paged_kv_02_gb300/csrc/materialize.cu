@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kThreads) materialize_kernel(const Materialize
 // and bulk-copies the source page's codes and scales into the next free shared-memory
 // stage; the consumer warps convert from shared memory and stream the 32-byte stores.
 
-__global__ void __launch_bounds__(kTmaThreads, 2) materialize_tma_kernel(const MaterializeArgs a,
+__global__ void __launch_bounds__(kTmaThreads, 3) materialize_tma_kernel(const MaterializeArgs a,
                                                                        const TmaLayout L) {
   extern __shared__ __align__(128) uint8_t smem[];
   int32_t* s_cum = reinterpret_cast<int32_t*>(smem);

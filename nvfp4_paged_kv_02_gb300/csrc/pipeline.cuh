@@ -118,8 +118,9 @@ __host__ __device__ inline TmaLayout tma_layout(int B, uint32_t codes_bytes, uin
   return L;
 }
 
-// Stages that fit in `budget` bytes, between 2 and 8.
-inline int stages_for(uint32_t codes_bytes, uint32_t sf_bytes, uint32_t budget = 96u * 1024u) {
+// Stages that fit in `budget` bytes, between 2 and 8 (64 KB leaves room for three CTAs
+// per SM).
+inline int stages_for(uint32_t codes_bytes, uint32_t sf_bytes, uint32_t budget = 64u * 1024u) {
   const uint32_t one = round_up(codes_bytes, 128) + round_up(sf_bytes, 128);
   int ns = static_cast<int>(budget / one);
   return ns < 2 ? 2 : (ns > 8 ? 8 : ns);

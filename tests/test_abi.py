@@ -192,3 +192,54 @@ def test_dev_scale_append_rejects_null_scales(lib):
           ctypes.c_void_p(FAKE), 16, ctypes.c_void_p(FAKE), None, 2, None, ctypes.c_void_p(FAKE),
           None, None, None)
     assert r == nv.ERR_INVALID_ARG and "scale" in err(lib)
+
+
+def kv_quantize(lib, **kw):
+    a = dict(x=FAKE, dt=1, rows=4, cols=128, stride=128, gs=FAKE, out=FAKE, recipe=None)
+    a.update(kw)
+    return lib.nvfp4_kv_quantize(ctypes.c_void_p(a["x"]) if a["x"] else None, a["dt"], a["rows"],
+                                 a["cols"], a["stride"],
+                                 ctypes.c_void_p(a["gs"]) if a["gs"] else None, a["recipe"],
+                                 ctypes.c_void_p(a["out"]), ctypes.c_void_p(FAKE), None, None)
+
+
+@pytest.mark.parametrize("kw,code,text", [
+    (dict(dt=7), nv.ERR_INVALID_ARG, "dtype"),
+    (dict(cols=40), nv.ERR_INVALID_ARG, "cols"),
+    (dict(cols=0), nv.ERR_INVALID_ARG, "cols"),
+    (dict(rows=-1), nv.ERR_INVALID_ARG, "rows"),
+    (dict(stride=64), nv.ERR_INVALID_ARG, "row_stride"),
+    (dict(x=FAKE + 8), nv.ERR_ALIGNMENT, "aligned"),
+    (dict(stride=132), nv.ERR_ALIGNMENT, "aligned"),
+    (dict(out=FAKE + 4), nv.ERR_ALIGNMENT, "aligned"),
+    (dict(gs=0), nv.ERR_INVALID_ARG, "null"),
+])
+def test_kv_quantize_rejects(lib, kw, code, text):
+    assert kv_quantize(lib, **kw) == code
+    assert text in err(lib)
+
+
+def kv_dequantize(lib, **kw):
+    a = dict(fp4=FAKE, rows=4, cols=128, gs=FAKE, out=FAKE, odt=1)
+    a.update(kw)
+    return lib.nvfp4_kv_dequantize(ctypes.c_void_p(a["fp4"]), ctypes.c_void_p(FAKE), a["rows"],
+                                   a["cols"], ctypes.c_void_p(a["gs"]) if a["gs"] else None,
+                                   ctypes.c_void_p(a["out"]), a["odt"], None, None)
+
+
+@pytest.mark.parametrize("kw,code,text", [
+    (dict(odt=3), nv.ERR_INVALID_ARG, "out_dtype"),
+    (dict(cols=24), nv.ERR_INVALID_ARG, "cols"),
+    (dict(rows=-2), nv.ERR_INVALID_ARG, "rows"),
+    (dict(fp4=FAKE + 4), nv.ERR_ALIGNMENT, "aligned"),
+    (dict(out=FAKE + 8), nv.ERR_ALIGNMENT, "aligned"),
+    (dict(gs=0), nv.ERR_INVALID_ARG, "null"),
+])
+def test_kv_dequantize_rejects(lib, kw, code, text):
+    assert kv_dequantize(lib, **kw) == code
+    assert text in err(lib)
+
+
+def test_empty_contiguous_ops_are_no_ops(lib):
+    assert kv_quantize(lib, rows=0) == nv.OK
+    assert kv_dequantize(lib, rows=0) == nv.OK
