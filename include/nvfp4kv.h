@@ -284,6 +284,25 @@ nvfp4_status nvfp4_kv_dequantize(const uint8_t* fp4, const uint8_t* sf, int64_t 
                                  int32_t cols, const float* global_scale, void* out,
                                  int32_t out_dtype, int32_t* dev_status, void* stream);
 
+/* Pack a resolved recipe into one int64, for logs and repro tooling
+ * ("flashinfer.quantization" index, "NVFP4 4over6 Recipes": nvfp4_4over6_code and its
+ * inverse nvfp4_4over6_from_code). The pages do not give the bit layout; this library's is
+ *   0            recipe NULL: standard NVFP4 (4over6 off)
+ *   bit 0        1: 4over6 on
+ *   bit 1        err_mode (0 MAE, 1 MSE)
+ *   bit 2        err_use_fast_math
+ *   bits 3..31   zero
+ *   bits 32..63  the binary32 bit pattern of e4m3_max
+ * Host only (no device work, no stream). An invalid recipe (the check every entry point
+ * makes) or a NULL `code` returns NVFP4_ERR_INVALID_ARG. */
+nvfp4_status nvfp4_4over6_code(const nvfp4_4over6_config* recipe, int64_t* code);
+
+/* Inverse of nvfp4_4over6_code: code 0 gives *is_4over6 = 0 (and leaves *recipe alone);
+ * otherwise *is_4over6 = 1 and *recipe is the packed recipe. A code outside the layout, or
+ * one that packs an invalid recipe, returns NVFP4_ERR_INVALID_ARG. */
+nvfp4_status nvfp4_4over6_from_code(int64_t code, int32_t* is_4over6,
+                                    nvfp4_4over6_config* recipe);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,6 +31,7 @@ __all__ = [
     "nvfp4_make_global_scale", "nvfp4_quantize_append_paged", "nvfp4_dequantize_paged",
     "nvfp4_materialize_fp8", "nvfp4_materialize_fp8_out_pages", "NVFP4KVMaterializer",
     "paged_caches", "LIB_PATH", "nvfp4_kv_quantize", "nvfp4_kv_dequantize",
+    "nvfp4_4over6_code", "nvfp4_4over6_from_code",
 ]
 
 LIB_PATH = _build.LIB_PATH
@@ -110,6 +111,10 @@ def load() -> ctypes.CDLL:
         L.nvfp4_materialize_fp8.argtypes = [
             _Cache, _Cache, i32, i32, i32, i32, vp, i32, i32, vp, i32, i32, vp, i64, vp, i64, vp,
             i32, vp, vp]
+        L.nvfp4_4over6_code.restype = i32
+        L.nvfp4_4over6_code.argtypes = [vp, vp]
+        L.nvfp4_4over6_from_code.restype = i32
+        L.nvfp4_4over6_from_code.argtypes = [i64, vp, vp]
         L.nvfp4_kv_quantize.restype = i32
         L.nvfp4_kv_quantize.argtypes = [vp, i32, i64, i32, i64, vp, vp, vp, vp, vp, vp]
         L.nvfp4_kv_dequantize.restype = i32
@@ -449,3 +454,23 @@ def nvfp4_kv_dequantize(fp4_data: torch.Tensor, block_scales: torch.Tensor, glob
         _ptr(fp4_data), _ptr(block_scales), rows, cols, _ptr(gs), _ptr(out),
         _dtype_code(out.dtype), _ptr(dev_status), _stream(fp4_data.device)))
     return out
+
+
+def nvfp4_4over6_code(config: Optional[NVFP44Over6Config]) -> int:
+    """Pack a resolved recipe (None = standard NVFP4) into the library's int64 code."""
+    code = ctypes.c_int64()
+    _check("nvfp4_4over6_code", load().nvfp4_4over6_code(_recipe(config), ctypes.byref(code)))
+    return code.value
+
+
+def nvfp4_4over6_from_code(code: int) -> Optional[NVFP44Over6Config]:
+    """Inverse of nvfp4_4over6_code: None for standard NVFP4, else the recipe."""
+    on = ctypes.c_int32()
+    c = _Config()
+    _check("nvfp4_4over6_from_code",
+           load().nvfp4_4over6_from_code(int(code), ctypes.byref(on), ctypes.byref(c)))
+    if not on.value:
+        return None
+    return NVFP44Over6Config(e4m3_max=float(c.e4m3_max),
+                             err_mode="MSE" if c.err_mode == 1 else "MAE",
+                             err_use_fast_math=bool(c.err_use_fast_math))

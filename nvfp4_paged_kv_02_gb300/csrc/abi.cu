@@ -274,6 +274,46 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_append_paged_dev_scale(
                      1.0f, k_scale, v_scale, recipe, dev_status, stream);
 }
 
+NVFP4_EXPORT nvfp4_status nvfp4_4over6_code(const nvfp4_4over6_config* recipe, int64_t* code) {
+  clear_error();
+  if (!code) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_4over6_code: code is null");
+  if (!recipe) {
+    *code = 0;
+    return NVFP4_OK;
+  }
+  if (nvfp4_status st = check_recipe(recipe)) return st;
+  uint32_t bits;
+  std::memcpy(&bits, &recipe->e4m3_max, sizeof(bits));
+  const uint64_t c = (static_cast<uint64_t>(bits) << 32) | 1u |
+                     (recipe->err_mode == NVFP4_ERR_MSE ? 2u : 0u) |
+                     (recipe->err_use_fast_math ? 4u : 0u);
+  *code = static_cast<int64_t>(c);
+  return NVFP4_OK;
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_4over6_from_code(int64_t code, int32_t* is_4over6,
+                                                 nvfp4_4over6_config* recipe) {
+  clear_error();
+  if (!is_4over6 || !recipe)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_4over6_from_code: null output pointer");
+  if (code == 0) {
+    *is_4over6 = 0;
+    return NVFP4_OK;
+  }
+  const uint64_t c = static_cast<uint64_t>(code);
+  if ((c & 1u) == 0 || (c & 0xFFFFFFF8u) != 0)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_4over6_from_code: not a recipe code");
+  nvfp4_4over6_config r;
+  const uint32_t bits = static_cast<uint32_t>(c >> 32);
+  std::memcpy(&r.e4m3_max, &bits, sizeof(bits));
+  r.err_mode = (c & 2u) ? NVFP4_ERR_MSE : NVFP4_ERR_MAE;
+  r.err_use_fast_math = (c & 4u) ? 1 : 0;
+  if (nvfp4_status st = check_recipe(&r)) return st;
+  *recipe = r;
+  *is_4over6 = 1;
+  return NVFP4_OK;
+}
+
 NVFP4_EXPORT nvfp4_status nvfp4_kv_quantize(const void* input, int32_t dtype, int64_t rows,
                                             int32_t cols, int64_t row_stride,
                                             const float* global_scale,
