@@ -417,11 +417,12 @@ struct RowDst {
   uint8_t* vs;
 };
 
+template <bool CONTIG>
 __device__ __forceinline__ RowDst resolve_row_dst(const AppendArgs& a, int64_t i) {
   RowDst d{nullptr, nullptr, nullptr, nullptr};
   const int64_t rd = a.layout == NVFP4_NHD ? static_cast<int64_t>(a.H) * (a.D / 2) : a.D / 2;
   const int64_t rs = a.layout == NVFP4_NHD ? static_cast<int64_t>(a.H) * a.nb : a.nb;
-  if (a.contig) {
+  if (CONTIG) {
     d.kd = a.kc.data + i * rd;
     d.ks = a.kc.sf + i * rs;
     return d;
@@ -462,9 +463,11 @@ inline AppendTmaLayout append_tma_layout(uint32_t rows, uint32_t row_bytes, uint
   return L;
 }
 
-template <bool BF16, int MODE>
+// NKV: tensors per stage, 2 (K and V, paged) or 1 (the contiguous form).
+template <bool BF16, int MODE, int NKV>
 __global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const AppendArgs a,
                                                                   const AppendTmaLayout L) {
+  constexpr uint32_t nkv = NKV;
   extern __shared__ __align__(128) uint8_t smem[];
   Tables& tab = *reinterpret_cast<Tables*>(smem + L.tables_off);
   uint8_t* stages = smem + L.stages_off;
@@ -490,7 +493,7 @@ __global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const Append
   const int64_t tiles = (a.nnz + L.rows - 1) / L.rows;
   const uint32_t tile_bytes = L.rows * L.row_bytes;
   const bool contiguous =
-      a.k_row_bytes == L.row_bytes && (L.nkv == 1 || a.v_row_bytes == L.row_bytes);
+      a.k_row_bytes == L.row_bytes && (nkv == 1 || a.v_row_bytes == L.row_bytes);
   if (warp == kConsumerWarps) {
     int s = 0;
     uint32_t phase = 0, round = 0;  // phase = parity of `round`, the stage's fill count
@@ -503,7 +506,7 @@ __global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const Append
       // Resolve this tile's destinations (a chain of dependent index loads, one row per
       // lane: at most 32 rows) while the consumers still work on the stage it will use.
       RowDst d{nullptr, nullptr, nullptr, nullptr};
-      if (static_cast<uint32_t>(lane) < nrows) d = resolve_row_dst(a, row0 + lane);
+      if (static_cast<uint32_t>(lane) < nrows) d = resolve_row_dst<NKV == 1>(a, row0 + lane);
       bool ok = true;
       if (lane == 0) ok = mbar_wait(empty + s, phase ^ 1u, a.pipe.wait_limit) && !*s_abort;
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -515,21 +518,21 @@ __global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const Append
         break;
       }
       uint8_t* st = stages + static_cast<uint32_t>(s) * L.stage_bytes;
-      RowDst* dst = reinterpret_cast<RowDst*>(st + L.nkv * tile_bytes);
+      RowDst* dst = reinterpret_cast<RowDst*>(st + nkv * tile_bytes);
       if (static_cast<uint32_t>(lane) < nrows) dst[lane] = d;
       __syncwarp();
-      if (lane == 0 && !withhold) mbar_arrive_expect_tx(full + s, L.nkv * nrows * L.row_bytes);
+      if (lane == 0 && !withhold) mbar_arrive_expect_tx(full + s, nkv * nrows * L.row_bytes);
       __syncwarp();
       if (contiguous) {
         if (lane == 0 && nrows > 0) {
           bulk_g2s(st, a.k + row0 * a.k_row_bytes, nrows * L.row_bytes, full + s);
-          if (L.nkv == 2)
+          if (nkv == 2)
             bulk_g2s(st + tile_bytes, a.v + row0 * a.v_row_bytes, nrows * L.row_bytes, full + s);
         }
       } else if (static_cast<uint32_t>(lane) < nrows) {
         const uint32_t r = lane;
         bulk_g2s(st + r * L.row_bytes, a.k + (row0 + r) * a.k_row_bytes, L.row_bytes, full + s);
-        if (L.nkv == 2)
+        if (nkv == 2)
           bulk_g2s(st + tile_bytes + r * L.row_bytes, a.v + (row0 + r) * a.v_row_bytes,
                    L.row_bytes, full + s);
       }
@@ -566,7 +569,7 @@ __global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const Append
         break;
       }
       const uint8_t* st = stages + static_cast<uint32_t>(s) * L.stage_bytes;
-      const RowDst* dst = reinterpret_cast<const RowDst*>(st + L.nkv * tile_bytes);
+      const RowDst* dst = reinterpret_cast<const RowDst*>(st + nkv * tile_bytes);
       const int32_t nrows =
           static_cast<int32_t>(min(static_cast<int64_t>(L.rows), a.nnz - tile * L.rows));
       const int32_t nblk = nrows * row_blocks;
@@ -582,7 +585,7 @@ __global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const Append
         }
         const RowDst d = dst[r];
 #pragma unroll
-        for (int kv = 0; kv < 2; ++kv) {
+        for (int kv = 0; kv < NKV; ++kv) {
           uint8_t* pd = kv ? d.vd : d.kd;
           if (pd == nullptr) continue;
           const U32x8 x = ld_shared_256(st + kv * tile_bytes + 32 * k);
@@ -626,7 +629,7 @@ nvfp4_status launch_t(const AppendArgs& a, cudaStream_t stream) {
 template <bool BF16, int MODE>
 nvfp4_status launch_tma(const AppendArgs& a, uint32_t row_bytes, uint32_t nkv,
                         cudaStream_t stream) {
-  const auto kern = append_tma_kernel<BF16, MODE>;
+  const auto kern = nkv == 2 ? append_tma_kernel<BF16, MODE, 2> : append_tma_kernel<BF16, MODE, 1>;
   uint32_t rows = (nkv == 2 ? 16384u : 32768u) / row_bytes;
   rows = rows < 1 ? 1 : (rows > 32 ? 32 : rows);
   const uint32_t one = round_up(nkv * rows * row_bytes + rows * sizeof(RowDst), 128);
