@@ -70,6 +70,20 @@ def op_bytes(w: W.Workload, n_active_pages: int):
 
 
 # ---------------------------------------------------------------------------------------
+# replicas: the slowest rank's time
+# ---------------------------------------------------------------------------------------
+
+def max_over_ranks(x: float, dev: torch.device) -> float:
+    """The largest value of x over all ranks (x itself when not running distributed)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------------
 # DRAM traffic of a kernel, from a committed ncu summary
 # ---------------------------------------------------------------------------------------
 
@@ -546,12 +560,9 @@ def main():
         else:  # the device time of the ops, without the flushes between them
             step_ms.append(sum(evs[s][2 * i].elapsed_time(evs[s][2 * i + 1])
                                for i in range(n_ops)))
-    ms = float(np.mean(step_ms))
+    ms = max_over_ranks(float(np.mean(step_ms)), dev)
     if world > 1:
         import torch.distributed as dist
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
         dist.barrier()
     # per-op device time (mean over steps)
     seg = {k: (2 * i, 2 * i + 1) for i, k in enumerate(step.NAMES)}
@@ -634,12 +645,7 @@ def measure_e2e(step: Step, w: W.Workload, args, total_bytes: int, world: int):
         one()
     b.record()
     torch.cuda.synchronize(dev)
-    ms = a.elapsed_time(b) / n
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(a.elapsed_time(b) / n, dev)
     h2d = hk.numel() * hk.element_size() + hv.numel() * hv.element_size()
     return {"value": world * total_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 12, "ms_per_step": ms}
