@@ -41,6 +41,13 @@ METRIC = "HBM GB/s (% of 8 TB/s) and tokens/s per op: append, dequant_paged, mat
 NOMINAL_HBM_GBS = 8000.0
 
 
+def arith_dtype(w: W.Workload) -> str:
+    """The arithmetic the path computes in: binary32 everywhere, plus binary16 for the
+    4over6 error under the fast-math recipe."""
+    r = w.recipe
+    return "f32+f16" if r is not None and r.err_use_fast_math else "f32"
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -461,7 +468,8 @@ def reference_arm(args, w: W.Workload):
     v = nbytes / dt / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": arith_dtype(w),
             "data": "synthetic", "config": sample_cfg,
             "cpu_baseline": {"value": v, "unit": "GB/s", "cores": oracle.max_threads(),
                              "kind": "oracle",
@@ -591,7 +599,8 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": arith_dtype(w),
             "data": "synthetic",
             "config": {**step.config(),
                        "l2": "flushed before every op (256 MB write, then 256 MB read), "
