@@ -291,3 +291,37 @@ def test_append_with_device_scales():
         torch.cuda.synchronize()
         assert int(st.item()) == nv.DEV_BAD_SCALE
         assert (kd == 0xA5).all() and (ks == 0xA5).all()
+
+
+@pytest.mark.parametrize("what", ["wide_rows", "sf_stride_not_16", "big_pages"])
+def test_direct_load_kernels(what):
+    """Shapes the shared-memory ring cannot take run the direct-load kernels: an append row
+    of more than 24 KB per tensor (16 heads x 1024), scale pages whose stride is not a
+    multiple of 16 bytes (no bulk copy), and pages larger than a 48 KB stage (128 slots x 8
+    heads x 128)."""
+    if what == "wide_rows":
+        w = W.random_case(700, B=3, H=16, D=1024, ps=4, layout=W.NHD, dtype=torch.bfloat16,
+                          recipe=R_MAE16, max_len=9)
+        kw = {}
+    elif what == "sf_stride_not_16":
+        w = W.random_case(701, B=5, H=4, D=128, ps=16, layout=W.HND, dtype=torch.float16,
+                          recipe=R_MSE, max_len=70)
+        kw = dict(pad_data=16, pad_sf=8)
+    else:
+        w = W.random_case(702, B=3, H=8, D=128, ps=128, layout=W.HND, dtype=torch.bfloat16,
+                          recipe=R_STD, max_len=300)
+        kw = {}
+    g = PL.run_gpu(w, **kw)
+    o = PL.run_oracle(w, **kw)
+    PL.assert_same(g, o, what)
+
+
+def test_largest_batch():
+    """16384 requests (the largest batch a CTA's shared-memory scan takes), lengths 0..5."""
+    lens = np.arange(16384) % 6
+    w = W.make_paged("maxbatch", 9, B=16384, H=1, D=64, ps=4, layout=W.HND,
+                     dtype=torch.bfloat16, lens_old=np.zeros(16384, np.int64), lens_new=lens,
+                     extra_pages=3)
+    g = PL.run_gpu(w)
+    o = PL.run_oracle(w)
+    PL.assert_same(g, o, "max batch")
