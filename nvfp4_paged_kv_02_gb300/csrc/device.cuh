@@ -146,11 +146,6 @@ __device__ __forceinline__ uint64_t fadd2_rn(uint64_t a, uint64_t b) {
 // (ptxas was seen to fuse a packed mul.rn.f32x2 -- and an fma with a literal -0 addend --
 // into the next packed add despite the .rn modifier and -fmad=false, which changes the
 // rounding of an error sum.)
-__device__ __forceinline__ uint64_t fsq2_rn(uint64_t a, uint64_t nz) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %1, %2;" : "=l"(r) : "l"(a), "l"(nz));
-  return r;
-}
 __device__ __forceinline__ uint32_t hsq2_rn(uint32_t a, uint32_t nz) {
   uint32_t r;
   asm("fma.rn.f16x2 %0, %1, %1, %2;" : "=r"(r) : "r"(a), "r"(nz));

@@ -55,7 +55,7 @@ struct AppendArgs {
   float gs[2];
   const float* gs_dev[2];  // when set, the scales are read from device memory instead
   float cap_a;
-  uint32_t neg_zero;  // 0x80000000 (-0.0f), passed at run time for fsq2_rn / hsq2_rn
+  uint32_t neg_zero;  // 0x80000000 (-0.0f), passed at run time for hsq2_rn
   PipeTest pipe;
   int32_t* status;
   // Contiguous form (nvfp4_kv_quantize): row i goes to kc.data + i * H*D/2 and
