@@ -325,3 +325,51 @@ def test_largest_batch():
     g = PL.run_gpu(w)
     o = PL.run_oracle(w)
     PL.assert_same(g, o, "max batch")
+
+
+@pytest.mark.parametrize("recipe", [R_STD, R_MAE16, R_MSE])
+def test_append_order_split_and_repeat(recipe):
+    """Rows appended in any order, split over several calls, or appended twice, leave the
+    same bytes in the cache as one in-order call; the result is also the oracle's."""
+    import nvfp4_paged_kv_02_gb300 as nv
+    dev = torch.device("cuda")
+    w = W.random_case(800, B=6, H=4, D=128, ps=16, layout=W.HND, dtype=torch.bfloat16,
+                      recipe=recipe, max_len=120, min_len=10, prefill_frac=0.0)
+    r = PL.gpu_recipe(recipe)
+    t = lambda a: torch.as_tensor(np.ascontiguousarray(a)).to(dev)
+    gk = float(nv.nvfp4_make_global_scale(w.k.to(dev).contiguous(), r).item())
+    gv = float(nv.nvfp4_make_global_scale(w.v.to(dev).contiguous(), r).item())
+    shape = (w.num_pages, w.H, w.ps)
+
+    def fresh():
+        return ((torch.full((*shape, w.D // 2), 0xA5, dtype=torch.uint8, device=dev),
+                 torch.full((*shape, w.D // 2), 0xA5, dtype=torch.uint8, device=dev)),
+                (torch.full((*shape, w.D // 16), 0xA5, dtype=torch.uint8, device=dev),
+                 torch.full((*shape, w.D // 16), 0xA5, dtype=torch.uint8, device=dev)))
+
+    def append(cache, rows):
+        rows = np.asarray(rows, np.int64)
+        idx = torch.from_numpy(rows)
+        nv.nvfp4_quantize_append_paged(
+            w.k[idx].to(dev), w.v[idx].to(dev), t(w.batch_indices[rows]), t(w.positions[rows]),
+            cache[0], cache[1], t(w.kv_indices), t(w.kv_indptr), t(w.kv_last_page_len), gk, gv,
+            "HND", r)
+
+    def host(cache):
+        return [x.cpu().numpy() for pair in cache for x in pair]
+
+    order = np.arange(w.nnz)
+    base = fresh()
+    append(base, order)
+    want = host(base)
+    perm = np.random.default_rng(8).permutation(w.nnz)
+    for rows_list in ([perm], [order[: w.nnz // 3], order[w.nnz // 3:]],
+                      [perm[::2], perm[1::2]], [order, order]):
+        c = fresh()
+        for rows in rows_list:
+            append(c, rows)
+        for a, b in zip(host(c), want):
+            assert np.array_equal(a, b)
+    o = PL.run_oracle(w, do_dequant=False, do_materialize=False)
+    assert np.array_equal(want[0].reshape(-1), o.k_data) and np.array_equal(want[1].reshape(-1), o.v_data)
+    assert np.array_equal(want[2].reshape(-1), o.k_sf) and np.array_equal(want[3].reshape(-1), o.v_sf)
