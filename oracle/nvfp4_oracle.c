@@ -231,10 +231,11 @@ static double tree16_f16(double t[16]) {
   return t[0];
 }
 
-/* Reconstruction error of a candidate ([P4]: "quantizes the block with both, dequantizes
- * both"). Reading: the element error is x - e2m1(q)*S*gs computed exactly and rounded once
- * (a fused multiply-add) -- "exactly in fp32"; the summed term is |e| (MAE) or e*e rounded
- * (MSE). With fast math ([P4] err_use_fast_math: the error "in fp16") every step is a
+/* Reconstruction error of a candidate ([P4]: each candidate is quantized and then
+ * dequantized, and the reconstructions are compared). Reading: the element error is
+ * x - e2m1(q)*S*gs computed exactly and rounded once (a fused multiply-add), as the page
+ * calls the fp32 evaluation exact; the summed term is |e| (MAE) or e*e rounded (MSE).
+ * With fast math ([P4] err_use_fast_math, a half-precision evaluation) every step is a
  * binary16 operation: x and gs are rounded to binary16, the block's decode factor is
  * sg = RN16(S * gs_h), the element error is e = RN16(x_h - e2m1(q) * sg) (fused), and e*e
  * and each partial sum are rounded to binary16. */
