@@ -27,6 +27,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -547,8 +548,9 @@ def main():
         flush.fill_(flushes[0] & 0xFF)
         flush_read.sum()
 
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-    clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv"))
+    fd, clock_path = tempfile.mkstemp(prefix=f"nvfp4kv_clocks_rank{rank}_", suffix=".csv")
+    os.close(fd)
+    clocks = ClockSampler(clock_path)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
