@@ -461,10 +461,14 @@ inline AppendTmaLayout append_tma_layout(uint32_t rows, uint32_t row_bytes, uint
   return L;
 }
 
+// CTAs per SM by recipe: the binary32-error recipes (more arithmetic per block) run two
+// CTAs with more registers and 1.5x larger tiles, the others three (measured).
+constexpr int append_ctas_per_sm(int mode) { return (mode == 1 || mode == 2) ? 2 : 3; }
+
 // NKV: tensors per stage, 2 (K and V, paged) or 1 (the contiguous form).
 template <bool BF16, int MODE, int NKV>
-__global__ void __launch_bounds__(kTmaThreads, 3) append_tma_kernel(const AppendArgs a,
-                                                                  const AppendTmaLayout L) {
+__global__ void __launch_bounds__(kTmaThreads, append_ctas_per_sm(MODE))
+    append_tma_kernel(const AppendArgs a, const AppendTmaLayout L) {
   constexpr uint32_t nkv = NKV;
   extern __shared__ __align__(128) uint8_t smem[];
   Tables& tab = *reinterpret_cast<Tables*>(smem + L.tables_off);
@@ -623,15 +627,17 @@ nvfp4_status launch_t(const AppendArgs& a, cudaStream_t stream) {
 }
 
 // TMA path: tiles of up to 32 rows (the producer gives each row one lane) and about 16 KB
-// per tensor, 2 to 6 stages in 70 KB (three CTAs per SM).
+// per tensor, 2 to 6 stages in 70 KB (three CTAs per SM); for the binary32-error recipes
+// about 24 KB per tensor in 100 KB (two CTAs per SM).
 template <bool BF16, int MODE>
 nvfp4_status launch_tma(const AppendArgs& a, uint32_t row_bytes, uint32_t nkv,
                         cudaStream_t stream) {
   const auto kern = nkv == 2 ? append_tma_kernel<BF16, MODE, 2> : append_tma_kernel<BF16, MODE, 1>;
-  uint32_t rows = (nkv == 2 ? 16384u : 32768u) / row_bytes;
+  const bool two = append_ctas_per_sm(MODE) == 2;
+  uint32_t rows = (two ? 24576u : 16384u) * (nkv == 2 ? 1u : 2u) / row_bytes;
   rows = rows < 1 ? 1 : (rows > 32 ? 32 : rows);
   const uint32_t one = round_up(nkv * rows * row_bytes + rows * sizeof(RowDst), 128);
-  int ns = static_cast<int>((70u * 1024u) / one);
+  int ns = static_cast<int>((two ? 100u : 70u) * 1024u / one);
   ns = ns < 2 ? 2 : (ns > 6 ? 6 : ns);
   const AppendTmaLayout L = append_tma_layout(rows, row_bytes, nkv, ns);
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
