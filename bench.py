@@ -369,12 +369,21 @@ def active_pages(w: W.Workload) -> int:
 # the CPU oracle on a bounded sample (baseline and reference arm)
 # ---------------------------------------------------------------------------------------
 
-def oracle_sample(w: W.Workload, n_req: int):
+def oracle_sample(w: W.Workload, n_req: int, max_tokens: int = 0):
     """A sub-batch of the workload (its first n_req requests, their rows, a compact pool)
-    as host arrays, plus its algorithmic bytes."""
+    as host arrays, plus its algorithmic bytes. With max_tokens > 0 the sample instead
+    takes whole requests in order until max_tokens rows, the last one cut short."""
+    lens_all = w.seq_lens.astype(np.int64)
+    if max_tokens > 0:
+        cum = np.cumsum(lens_all)
+        n_req = int(np.searchsorted(cum, max_tokens)) + 1
+        n_req = min(n_req, w.B)
     sel = np.arange(min(n_req, w.B))
-    lens = w.seq_lens[sel].astype(np.int64)
-    rows = np.isin(w.batch_indices, sel)
+    lens = lens_all[sel].copy()
+    if max_tokens > 0:
+        before = int(lens[:-1].sum())
+        lens[-1] = max(1, min(lens[-1], max_tokens - before))
+    rows = np.isin(w.batch_indices, sel) & (w.positions < lens[np.minimum(w.batch_indices, len(sel) - 1)])
     sub = W.make_paged("sample", 0, B=len(sel), H=w.H, D=w.D, ps=w.ps, layout=w.layout,
                        dtype=w.dtype, lens_old=np.zeros(len(sel), np.int64), lens_new=lens,
                        recipe=w.recipe, sampler=lambda r, n: np.zeros((n, w.H, w.D), np.float32),
@@ -450,18 +459,27 @@ def reference_arm(args, w: W.Workload):
     """The CPU oracle as the reference implementation: K timed steps (after W untimed) on a
     bounded sample of the same workload."""
     import oracle
+    # size one step's sample so that all W + K steps take about two minutes
+    per_step = 120.0 / max(1, args.steps + args.warmup)
     if args.workload == "contig":
-        n_rows = 8192 * max(1, args.ref_requests)
+        kv, _ = contig_sample(w, 8192)
+        t1 = time_oracle_contig(kv, w.recipe)
+        n_rows = int(max(64, min(w.nnz, 8192 * per_step / max(t1, 1e-4))))
         kv, nbytes = contig_sample(w, n_rows)
         timer = lambda: time_oracle_contig(kv, w.recipe)
         sample = f"first {kv[0].shape[0]} of {w.nnz} K and V rows"
         sample_cfg = {"workload": "contig", "sample_rows": kv[0].shape[0]}
     else:
-        n_req = max(1, min(w.B, args.ref_requests))
-        sub, nbytes = oracle_sample(w, n_req)
+        probe, _ = oracle_sample(w, 0, max_tokens=2048)
+        t1 = time_oracle(probe)
+        probe_tok = int(probe.seq_lens.astype(np.int64).sum())
+        all_tok = int(w.seq_lens.astype(np.int64).sum())
+        n_tok = int(max(16, min(all_tok, probe_tok * per_step / max(t1, 1e-4))))
+        sub, nbytes = oracle_sample(w, 0, max_tokens=n_tok)
         timer = lambda: time_oracle(sub)
-        sample = f"first {n_req} of {w.B} requests ({sub.nnz} tokens)"
-        sample_cfg = {"workload": w.name, "sample_requests": n_req, "sample_tokens": sub.nnz}
+        n_s = int(sub.seq_lens.astype(np.int64).sum())
+        sample = f"first {n_s} of {all_tok} cached tokens (first {sub.B} of {w.B} requests)"
+        sample_cfg = {"workload": w.name, "sample_requests": sub.B, "sample_tokens": n_s}
     for _ in range(args.warmup):
         timer()
     times = [timer() for _ in range(args.steps)]
@@ -489,7 +507,6 @@ def main():
     ap.add_argument("--workload", default="large_pool",
                     choices=["large_pool", "decode", "prefill", "materialize", "tiny", "contig"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--ref-requests", type=int, default=4)
     ap.add_argument("--batch", type=int, default=256, help="large_pool: requests")
     ap.add_argument("--pool-gb", type=float, default=W.LARGE_POOL_BYTES / 1e9,
                     help="large_pool: pool size (K+V codes and scales), GB")
