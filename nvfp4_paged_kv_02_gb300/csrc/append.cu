@@ -5,8 +5,10 @@
 // index (two-candidate block-scale search, e4m3_max, err_mode, err_use_fast_math).
 //
 // One thread quantizes one 16-element block of one (token, head) row, for K and for V: the
-// two blocks share the page lookup and give each thread two independent 32-byte loads in
-// flight. A warp covers 32 consecutive blocks, i.e. 1 KB of contiguous input.
+// two blocks share the destination lookup and give the thread two independent chains of
+// work. The main kernel is fed by a TMA ring (tiles of consecutive rows in shared memory);
+// the direct-load kernel, for rows too long for a stage, reads the blocks from global
+// memory, a warp covering 32 consecutive blocks (1 KB of contiguous input).
 //
 // Per block and candidate scale byte s (S = E4M3 value, gs = global decode scale):
 //   inv = 1 / (S * gs)      (binary32 reciprocal; 0 when S*gs is 0; at most FLT_MAX)
@@ -19,9 +21,9 @@
 //                   binary16, the rest is one fused multiply-add);
 //   binary16 error: e_i = RN16(x_h - e2m1(q_i) * sg) with x_h = RN16(x_i) and
 //                   sg = RN16(S * RN16(gs)); squares and sums rounded to binary16.
-// The sum runs over a fixed halving tree: t[i] += t[i+8], t[i+4], t[i+2], t[i+1], which
-// is exactly the order of the packed two-lane adds. B is kept only when its error is
-// strictly smaller.
+// The sum runs over a fixed halving tree: t[i] += t[i+8], t[i+4], t[i+2], t[i+1] (the
+// binary16 sums run it as packed two-lane adds, pairs (2k, 2k+1)). B is kept only when its
+// error is strictly smaller.
 //
 // Per-CTA shared tables, indexed by scale byte: 1/(S*gs) (both tensors), (S, S) as half2,
 // and -sg as half2 (both tensors).

@@ -25,21 +25,6 @@ namespace nvfp4 {
 
 // ---- packed format conversions --------------------------------------------------------
 
-// Eight binary32 values (in element order) -> four bytes of E2M1 codes.
-__device__ __forceinline__ uint32_t e2m1x8_from_f32(float v0, float v1, float v2, float v3,
-                                                    float v4, float v5, float v6, float v7) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
-      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
-      : "=r"(r)
-      : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7));
-  return r;
-}
-
 // Four bytes of E2M1 codes -> four half2 (byte k -> h[k], low nibble in .x).
 __device__ __forceinline__ void f16x2x4_from_e2m1x8(uint32_t w, uint32_t& h0, uint32_t& h1,
                                                     uint32_t& h2, uint32_t& h3) {
@@ -96,7 +81,6 @@ __device__ __forceinline__ float f32_from_f16_hi(uint32_t h) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(h >> 16)));
 }
 // Exact binary32 value of the two bf16 halves of a word.
-__device__ __forceinline__ float f32_from_bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float f32_from_bf16_hi(uint32_t w) {
   return __uint_as_float(w & 0xFFFF0000u);
 }
@@ -119,33 +103,13 @@ __device__ __forceinline__ uint32_t hfma2_rn(uint32_t a, uint32_t b, uint32_t c)
   return r;
 }
 
-// ---- packed binary32 arithmetic (sm_100+ f32x2 forms; two lanes per instruction) -------
-
-__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void f32x2_unpack(uint64_t p, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(p));
-}
-__device__ __forceinline__ uint64_t fmul2_rn(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t fadd2_rn(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-
 // Squares written as a fused multiply-add whose addend `nz` is -0 at run time:
 // RN(a*a + -0) == RN(a*a), one rounding. The compiler cannot see that the addend is -0, so
 // it can neither turn the FMA back into a multiply nor contract it into a following add.
-// (ptxas was seen to fuse a packed mul.rn.f32x2 -- and an fma with a literal -0 addend --
-// into the next packed add despite the .rn modifier and -fmad=false, which changes the
+// (ptxas was seen to fuse a packed square -- and an fma with a literal -0 addend -- into
+// the next packed add despite the .rn modifier and -fmad=false, which changes the
 // rounding of an error sum.)
+// ---- scalar helpers -----------------------------------------------------------------------
 __device__ __forceinline__ uint32_t hsq2_rn(uint32_t a, uint32_t nz) {
   uint32_t r;
   asm("fma.rn.f16x2 %0, %1, %1, %2;" : "=r"(r) : "r"(a), "r"(nz));
