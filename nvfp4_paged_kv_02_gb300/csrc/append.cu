@@ -463,14 +463,23 @@ inline AppendTmaLayout append_tma_layout(uint32_t rows, uint32_t row_bytes, uint
   return L;
 }
 
-// CTAs per SM by recipe: the binary32-error recipes (more arithmetic per block) run two
-// CTAs with more registers and 1.5x larger tiles, the others three (measured).
-constexpr int append_ctas_per_sm(int mode) { return (mode == 1 || mode == 2) ? 2 : 3; }
+// TMA ring shape (measured): two CTAs per SM with 12-row tiles; twelve consumer warps,
+// except for the binary32-error recipes (more arithmetic and registers per block), which
+// run eight.
+__host__ __device__ constexpr int append_consumer_warps(int mode) {
+  return (mode == 1 || mode == 2) ? 8 : 12;
+}
+__host__ __device__ constexpr int append_threads(int mode) {
+  return 32 * append_consumer_warps(mode) + 32;
+}
+constexpr int kAppendCtasPerSm = 2;
 
 // NKV: tensors per stage, 2 (K and V, paged) or 1 (the contiguous form).
 template <bool BF16, int MODE, int NKV>
-__global__ void __launch_bounds__(kTmaThreads, append_ctas_per_sm(MODE))
+__global__ void __launch_bounds__(append_threads(MODE), kAppendCtasPerSm)
     append_tma_kernel(const AppendArgs a, const AppendTmaLayout L) {
+  constexpr int kConsumerWarps = append_consumer_warps(MODE);
+  constexpr int kConsumers = kConsumerWarps * 32;
   constexpr uint32_t nkv = NKV;
   extern __shared__ __align__(128) uint8_t smem[];
   Tables& tab = *reinterpret_cast<Tables*>(smem + L.tables_off);
@@ -628,28 +637,27 @@ nvfp4_status launch_t(const AppendArgs& a, cudaStream_t stream) {
   return check_launch("nvfp4_quantize_append_paged");
 }
 
-// TMA path: tiles of up to 32 rows (the producer gives each row one lane) and about 16 KB
-// per tensor, 2 to 6 stages in 70 KB (three CTAs per SM); for the binary32-error recipes
-// about 24 KB per tensor in 100 KB (two CTAs per SM).
+// TMA path: tiles of up to 32 rows (the producer gives each row one lane) and about 24 KB
+// per tensor, 2 to 6 stages in 100 KB (two CTAs per SM).
 template <bool BF16, int MODE>
 nvfp4_status launch_tma(const AppendArgs& a, uint32_t row_bytes, uint32_t nkv,
                         cudaStream_t stream) {
   const auto kern = nkv == 2 ? append_tma_kernel<BF16, MODE, 2> : append_tma_kernel<BF16, MODE, 1>;
-  const bool two = append_ctas_per_sm(MODE) == 2;
-  uint32_t rows = (two ? 24576u : 16384u) * (nkv == 2 ? 1u : 2u) / row_bytes;
+  uint32_t rows = 24576u * (nkv == 2 ? 1u : 2u) / row_bytes;
   rows = rows < 1 ? 1 : (rows > 32 ? 32 : rows);
   const uint32_t one = round_up(nkv * rows * row_bytes + rows * sizeof(RowDst), 128);
-  int ns = static_cast<int>((two ? 100u : 70u) * 1024u / one);
+  int ns = static_cast<int>(100u * 1024u / one);
   ns = ns < 2 ? 2 : (ns > 6 ? 6 : ns);
   const AppendTmaLayout L = append_tma_layout(rows, row_bytes, nkv, ns);
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(L.total));
   const int64_t tiles = (a.nnz + rows - 1) / rows;
   const int64_t cap = static_cast<int64_t>(sm_count()) *
-                      blocks_per_sm(reinterpret_cast<const void*>(kern), kTmaThreads, L.total);
+                      blocks_per_sm(reinterpret_cast<const void*>(kern), append_threads(MODE),
+                                    L.total);
   const int grid = static_cast<int>(tiles < cap ? tiles : cap);
   if (grid <= 0) return NVFP4_OK;
-  kern<<<grid, kTmaThreads, L.total, stream>>>(a, L);
+  kern<<<grid, append_threads(MODE), L.total, stream>>>(a, L);
   return check_launch("nvfp4_quantize_append_paged");
 }
 

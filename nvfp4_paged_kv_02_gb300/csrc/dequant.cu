@@ -19,6 +19,11 @@
 namespace nvfp4 {
 namespace {
 
+// TMA ring shape: eight consumer warps, three CTAs per SM.
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kTmaThreads = kConsumers + 32;
+
 // 128-thread CTAs (about a dozen resident per SM) each load a whole 16-token page's blocks
 // per thread before decoding, so many pages' loads are in flight at once.
 constexpr int kThreads = 128;

@@ -19,6 +19,11 @@
 namespace nvfp4 {
 namespace {
 
+// TMA ring shape: twelve consumer warps, three CTAs per SM (measured faster than eight).
+constexpr int kConsumerWarps = 12;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kTmaThreads = kConsumers + 32;
+
 // 128-thread CTAs (about a dozen resident per SM): each thread loads its four chunks of a
 // 16-token page before converting, and many pages are in flight per SM.
 constexpr int kThreads = 128;

@@ -83,11 +83,8 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 //
 // Dynamic shared memory: [per-request scan: B int32][ns stages: codes | scales]
 // [ns StageMeta][ns full + ns empty mbarriers][abort flag][ns issue counters].
-// Warp kConsumerWarps produces (bulk copies), warps 0..kConsumerWarps-1 consume.
-
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kTmaThreads = kConsumers + 32;
+// Each kernel file sets its ring's shape: warps 0..W-1 consume, warp W produces (bulk
+// copies), so a CTA has 32 * W + 32 threads.
 
 struct StageMeta {
   int32_t f0, f1, f2, flags;  // item fields chosen by the kernel; flags bit 1 = page valid
