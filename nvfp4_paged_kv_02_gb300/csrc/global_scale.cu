@@ -6,7 +6,8 @@
 // so that the block holding the tensor's amax gets the top block scale e4m3_max.
 //
 // The amax is exact: |x| of fp16/bf16 orders like the integer (bits & 0x7FFF), so the scan
-// takes unsigned 16-bit maxima of the masked words (two per 32-bit lane op), reduces over
+// takes unsigned 16-bit maxima of the masked words (two per 32-bit lane op; four 32-byte
+// loads in flight per thread), reduces over
 // the CTA and combines CTAs with an atomic max on the binary32 bit pattern of the result,
 // accumulated in the output word itself (zeroed by a memset first). A one-thread kernel
 // then turns the amax into gs.
@@ -29,8 +30,17 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* __restri
   uint32_t m2 = 0;  // two 16-bit maxima
   const int64_t nvec = numel / 16;
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec;
-       v += step) {
+  int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; v + 3 * step < nvec; v += 4 * step) {
+    U32x8 w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) w[u] = ld_nc_2x128(x + (v + u * step) * 16);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m2 = __vmaxu2(m2, w[u].w[k] & 0x7FFF7FFFu);
+  }
+  for (; v < nvec; v += step) {
     const U32x8 w = ld_nc_2x128(x + v * 16);
 #pragma unroll
     for (int k = 0; k < 8; ++k) m2 = __vmaxu2(m2, w.w[k] & 0x7FFF7FFFu);
