@@ -697,9 +697,16 @@ def measure_e2e(step, w: W.Workload, args, total_bytes: int, world: int):
     step.k, step.v = bufs[0]
     ms = max_over_ranks(a.elapsed_time(b) / n, dev)
     h2d = hk.numel() * hk.element_size() + hv.numel() * hv.element_size()
+    # the host link alone: one copy of the K rows, for reading the e2e figure against
+    a.record(comp)
+    bufs[1][0].copy_(hk, non_blocking=True)
+    b.record(comp)
+    torch.cuda.synchronize(dev)
+    link = hk.numel() * hk.element_size() / (a.elapsed_time(b) * 1e-3) / 1e9
     return {"value": world * total_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 12, "ms_per_step": ms,
-            "pipelined": "copies of step i+1 overlap the compute of step i (two buffers)"}
+            "pipelined": "copies of step i+1 overlap the compute of step i (two buffers)",
+            "host_to_device_gbs": link}
 
 
 if __name__ == "__main__":
