@@ -474,8 +474,9 @@ __host__ __device__ constexpr int append_threads(int mode) {
 }
 constexpr int kAppendCtasPerSm = 2;
 
-// NKV: tensors per stage, 2 (K and V, paged) or 1 (the contiguous form).
-template <bool BF16, int MODE, int NKV>
+// NKV: tensors per stage, 2 (K and V, paged) or 1 (the contiguous form). FIXED: a row's
+// blocks divide the consumer threads (chosen at launch), so each thread keeps one (head, block).
+template <bool BF16, int MODE, int NKV, bool FIXED>
 __global__ void __launch_bounds__(append_threads(MODE), kAppendCtasPerSm)
     append_tma_kernel(const AppendArgs a, const AppendTmaLayout L) {
   constexpr int kConsumerWarps = append_consumer_warps(MODE);
@@ -566,7 +567,7 @@ __global__ void __launch_bounds__(append_threads(MODE), kAppendCtasPerSm)
     const int32_t hsd = a.layout == NVFP4_NHD ? a.D / 2 : a.ps * (a.D / 2);
     const int32_t hss = a.layout == NVFP4_NHD ? a.nb : a.ps * a.nb;
     // when a row's blocks divide the consumer count, each thread keeps one (head, block)
-    const bool fixed = kConsumers % row_blocks == 0;
+    constexpr bool fixed = FIXED;
     const int32_t fr0 = fixed ? ct / row_blocks : 0, frs = fixed ? kConsumers / row_blocks : 0;
     const int32_t frem = fixed ? ct - fr0 * row_blocks : 0;
     const int32_t fh = fixed ? frem / a.nb : 0, fj = fixed ? frem - fh * a.nb : 0;
@@ -642,7 +643,9 @@ nvfp4_status launch_t(const AppendArgs& a, cudaStream_t stream) {
 template <bool BF16, int MODE>
 nvfp4_status launch_tma(const AppendArgs& a, uint32_t row_bytes, uint32_t nkv,
                         cudaStream_t stream) {
-  const auto kern = nkv == 2 ? append_tma_kernel<BF16, MODE, 2> : append_tma_kernel<BF16, MODE, 1>;
+  const bool fx = append_consumer_warps(MODE) * 32 % (a.H * a.nb) == 0;
+  const auto kern = nkv == 2 ? (fx ? append_tma_kernel<BF16, MODE, 2, true> : append_tma_kernel<BF16, MODE, 2, false>)
+                             : (fx ? append_tma_kernel<BF16, MODE, 1, true> : append_tma_kernel<BF16, MODE, 1, false>);
   uint32_t rows = 24576u * (nkv == 2 ? 1u : 2u) / row_bytes;
   rows = rows < 1 ? 1 : (rows > 32 ? 32 : rows);
   const uint32_t one = round_up(nkv * rows * row_bytes + rows * sizeof(RowDst), 128);
