@@ -28,6 +28,7 @@
 // Per-CTA shared tables, indexed by scale byte: 1/(S*gs) (both tensors), (S, S) as half2,
 // and -sg as half2 (both tensors).
 #include <cfloat>
+#include <type_traits>
 
 #include "internal.h"
 #include "pipeline.cuh"
@@ -58,7 +59,10 @@ __device__ __forceinline__ TensorConsts make_consts(float gs) {
   return c;
 }
 
+// RN(a / b). EXACT: the caller knows that b and rb are normal (div_rn_with_rcp applies).
+template <bool EXACT>
 __device__ __forceinline__ float quotient(float a, float b, float rb, bool exact_rcp) {
+  if (EXACT) return div_rn_with_rcp(a, b, rb);
   return exact_rcp ? div_rn_with_rcp(a, b, rb) : __fdiv_rn(a, b);
 }
 
@@ -216,7 +220,7 @@ struct BlockOut {
   uint32_t c0, c1, s;
 };
 
-template <bool BF16, int MODE>
+template <bool BF16, int MODE, bool EXACT = false>
 __device__ __forceinline__ BlockOut quantize_block(const U32x8& in, const TensorConsts& tc,
                                                    const Tables& tab, int kv, float cap_a,
                                                    uint32_t nz) {
@@ -226,7 +230,7 @@ __device__ __forceinline__ BlockOut quantize_block(const U32x8& in, const Tensor
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-  const float ra = fminf(quotient(amax, tc.g6, tc.r6, tc.exact_rcp), cap_a);
+  const float ra = fminf(quotient<EXACT>(amax, tc.g6, tc.r6, tc.exact_rcp), cap_a);
   BlockOut r;
   if (MODE == 0) {
     r.s = e4m3x2_from_f32(ra, 0.0f) & 0xFFu;
@@ -235,7 +239,7 @@ __device__ __forceinline__ BlockOut quantize_block(const U32x8& in, const Tensor
     r.c1 = codes8(x + 8, inv);
     return r;
   }
-  const float rb = fminf(quotient(amax, tc.g4, tc.r4, tc.exact_rcp), 448.0f);
+  const float rb = fminf(quotient<EXACT>(amax, tc.g4, tc.r4, tc.exact_rcp), 448.0f);
   const uint32_t sab = e4m3x2_from_f32(ra, rb);
   // sb = sab >> 8 and sa = sab & 0xFF as multiplies (FMA pipe)
   uint32_t sb;
@@ -572,6 +576,11 @@ __global__ void __launch_bounds__(append_threads(MODE), kAppendCtasPerSm)
     const int32_t frem = fixed ? ct - fr0 * row_blocks : 0;
     const int32_t fh = fixed ? frem / a.nb : 0, fj = fixed ? frem - fh * a.nb : 0;
     const int32_t fod = fh * hsd + 8 * fj, fos = fh * hss + fj;
+    // The consumer loop is compiled twice: when both tensors' scale divisors and their
+    // reciprocals are normal (every realistic global scale), the quotients need no IEEE
+    // division fallback; the general form keeps it.
+    auto consume = [&](auto exact_tag) {
+    constexpr bool kExact = decltype(exact_tag)::value;
     int s = 0;
     uint32_t phase = 0;
     for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
@@ -604,7 +613,8 @@ __global__ void __launch_bounds__(append_threads(MODE), kAppendCtasPerSm)
           if (pd == nullptr) continue;
           const U32x8 x = ld_shared_256(st + kv * tile_bytes + 32 * k);
           const BlockOut q =
-              quantize_block<BF16, MODE>(x, kv ? tcv : tck, tab, kv, a.cap_a, a.neg_zero);
+              quantize_block<BF16, MODE, kExact>(x, kv ? tcv : tck, tab, kv, a.cap_a,
+                                                 a.neg_zero);
           *reinterpret_cast<uint2*>(pd + od) = make_uint2(q.c0, q.c1);
           (kv ? d.vs : d.ks)[os] = static_cast<uint8_t>(q.s);
         }
@@ -616,6 +626,9 @@ __global__ void __launch_bounds__(append_threads(MODE), kAppendCtasPerSm)
         phase ^= 1u;
       }
     }
+    };
+    if (tck.exact_rcp && tcv.exact_rcp) consume(std::integral_constant<bool, true>{});
+    else consume(std::integral_constant<bool, false>{});
   }
   // no copy may still be landing in this CTA's shared memory when it exits
   __syncthreads();

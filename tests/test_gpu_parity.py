@@ -373,3 +373,40 @@ def test_append_order_split_and_repeat(recipe):
     o = PL.run_oracle(w, do_dequant=False, do_materialize=False)
     assert np.array_equal(want[0].reshape(-1), o.k_data) and np.array_equal(want[1].reshape(-1), o.v_data)
     assert np.array_equal(want[2].reshape(-1), o.k_sf) and np.array_equal(want[3].reshape(-1), o.v_sf)
+
+
+@pytest.mark.parametrize("gk,gv", [(1e-40, 0.01), (0.02, 3e-39), (1e37, 1e38), (2.5e38, 1e-30),
+                                   (7e-39, 7e-39)])
+@pytest.mark.parametrize("recipe", [R_STD, R_MSE, R_MAE16])
+def test_extreme_global_scales(gk, gv, recipe):
+    """Global scales whose 6*gs or 4*gs (or their reciprocals) are subnormal or overflow take
+    the general division path; the result still matches the oracle (paged append and the
+    contiguous quantize)."""
+    import nvfp4_paged_kv_02_gb300 as nv
+    dev = torch.device("cuda")
+    gk, gv = float(np.float32(gk)), float(np.float32(gv))
+    w = W.random_case(900, B=3, H=2, D=64, ps=8, layout=W.NHD, dtype=torch.bfloat16,
+                      recipe=recipe, max_len=40, min_len=5, prefill_frac=0.0,
+                      scale_range=(1e-3, 1e3))
+    t = lambda a: torch.as_tensor(np.ascontiguousarray(a)).to(dev)
+    shape = (w.num_pages, w.ps, w.H)
+    kc = [torch.full((*shape, w.D // 2), 0xA5, dtype=torch.uint8, device=dev) for _ in range(2)]
+    ks = [torch.full((*shape, w.D // 16), 0xA5, dtype=torch.uint8, device=dev) for _ in range(2)]
+    nv.nvfp4_quantize_append_paged(w.k.to(dev), w.v.to(dev), t(w.batch_indices), t(w.positions),
+                                   tuple(kc), tuple(ks), t(w.kv_indices), t(w.kv_indptr),
+                                   t(w.kv_last_page_len), gk, gv, "NHD", PL.gpu_recipe(recipe))
+    dps, sps = PL.strides(w)
+    oc = [O.PagedCache(np.full(w.num_pages * dps, 0xA5, np.uint8),
+                       np.full(w.num_pages * sps, 0xA5, np.uint8), dps, sps) for _ in range(2)]
+    HD = w.H * w.D
+    O.quantize_append_paged(W.bits16(w.k), W.bits16(w.v), True, w.nnz, w.H, w.D, HD, HD,
+                            w.batch_indices, w.positions, oc[0], oc[1], w.ps, W.NHD,
+                            w.kv_indices, w.kv_indptr, gk, gv, PL.oracle_recipe(recipe))
+    for i in range(2):
+        assert np.array_equal(kc[i].cpu().numpy().reshape(-1), oc[i].data), i
+        assert np.array_equal(ks[i].cpu().numpy().reshape(-1), oc[i].sf), i
+    # contiguous form with the K scale
+    x = w.k.reshape(w.nnz, HD)
+    fp4, sf = nv.nvfp4_kv_quantize(x.to(dev), gk, PL.gpu_recipe(recipe))
+    c, s_ = O.kv_quantize(W.bits16(x), True, gk, PL.oracle_recipe(recipe))
+    assert np.array_equal(fp4.cpu().numpy(), c) and np.array_equal(sf.cpu().numpy(), s_)
