@@ -2,7 +2,8 @@
 
 Every shared-memory stage wait in the TMA-fed kernels is bounded. Here the host makes a
 wait run out: NVFP4KV_TEST_STALL_PIPELINE=1 makes each CTA's producer withhold its first
-stage (a barrier nothing completes) and shortens the wait limit. The call must come back
+stage (a barrier nothing completes) and shortens the wait limit. The contiguous quantize
+runs the append's pipeline and is checked the same way. The call must come back
 on its own with NVFP4_DEV_TIMEOUT set, and the CUDA context must stay usable: the same call
 without the switch then matches the CPU oracle.
 """
@@ -49,7 +50,7 @@ def test_stalled_pipelines_report_timeout_and_recover(stall_env):
     vd, vs = kd.clone(), ks.clone()
     g = torch.tensor([0.01], dtype=torch.float32, device=dev)
     r = PL.gpu_recipe(w.recipe)
-    for op in ("append", "dequant", "materialize"):
+    for op in ("append", "dequant", "materialize", "kv_quantize"):
         st = torch.zeros(1, dtype=torch.int32, device=dev)
         if op == "append":
             nv.nvfp4_quantize_append_paged(w.k.to(dev), w.v.to(dev), t(w.batch_indices),
@@ -59,9 +60,11 @@ def test_stalled_pipelines_report_timeout_and_recover(stall_env):
             ok = torch.zeros((w.B, w.max_seq_len, w.H, w.D), dtype=torch.bfloat16, device=dev)
             nv.nvfp4_dequantize_paged((kd, vd), (ks, vs), t(w.block_tables), t(w.seq_lens), g, g,
                                       ok, ok.clone(), "HND", st)
-        else:
+        elif op == "materialize":
             nv.nvfp4_materialize_fp8(kd, vd, ks, vs, t(w.mat_block_tables), t(w.seq_lens),
                                      w.max_kv_len, True, kv_layout="HND", dev_status=st)
+        else:  # the contiguous quantize shares the append's pipeline
+            nv.nvfp4_kv_quantize(w.k.to(dev).reshape(w.nnz, -1), g, r, dev_status=st)
         torch.cuda.synchronize()
         assert int(st.item()) & nv.DEV_TIMEOUT, (op, int(st.item()))
     # the context is still usable: a normal run matches the oracle
