@@ -102,7 +102,8 @@ KERNEL_SOURCES = {
     "kv_dequantize": ["dequant.cu"],
 }
 SHARED_SOURCES = ["device.cuh", "internal.h", "pipeline.cuh", "scan.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic_large_pool.md")
+TRAFFIC_FILES = [os.path.join(ROOT, "profiles", f)
+                 for f in ("dram_traffic_large_pool.md", "dram_traffic_contig.md")]
 
 
 def source_hash(op: str) -> str:
@@ -118,17 +119,18 @@ def traffic_per_launch(op: str, units: int):
     """DRAM bytes (read + write) per launch of the op's kernel: the bytes per unit that an ncu
     capture measured, times the units of this launch. None when there is no capture or the
     kernel's sources changed since it was taken."""
-    if not os.path.exists(TRAFFIC_FILE):
-        return None
     want = source_hash(op)
-    with open(TRAFFIC_FILE) as f:
-        for ln in f:
-            cells = [c.strip().strip("`") for c in ln.strip().strip("|").split("|")]
-            if len(cells) >= 6 and cells[0] == op and cells[1] == want:
-                try:
-                    return float(cells[5]) * units
-                except ValueError:
-                    return None
+    for path in TRAFFIC_FILES:
+        if not os.path.exists(path):
+            continue
+        with open(path) as f:
+            for ln in f:
+                cells = [c.strip().strip("`") for c in ln.strip().strip("|").split("|")]
+                if len(cells) >= 6 and cells[0] == op and cells[1] == want:
+                    try:
+                        return float(cells[5]) * units
+                    except ValueError:
+                        return None
     return None
 
 
