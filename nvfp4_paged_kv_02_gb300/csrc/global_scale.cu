@@ -6,7 +6,7 @@
 // so that the block holding the tensor's amax gets the top block scale e4m3_max.
 //
 // The amax is exact: |x| of fp16/bf16 orders like the integer (bits & 0x7FFF), so the scan
-// takes unsigned 16-bit maxima of the masked words (two per 32-bit lane op; four 32-byte
+// takes unsigned 16-bit maxima of the masked words (two per 32-bit lane op; eight 32-byte
 // loads in flight per thread), reduces over
 // the CTA and combines CTAs with an atomic max on the binary32 bit pattern of the result,
 // accumulated in the output word itself (zeroed by a memset first). A one-thread kernel
@@ -31,12 +31,12 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* __restri
   const int64_t nvec = numel / 16;
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
   int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (; v + 3 * step < nvec; v += 4 * step) {
-    U32x8 w[4];
+  for (; v + 7 * step < nvec; v += 8 * step) {
+    U32x8 w[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) w[u] = ld_nc_2x128(x + (v + u * step) * 16);
+    for (int u = 0; u < 8; ++u) w[u] = ld_nc_2x128(x + (v + u * step) * 16);
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < 8; ++u)
 #pragma unroll
       for (int k = 0; k < 8; ++k) m2 = __vmaxu2(m2, w[u].w[k] & 0x7FFF7FFFu);
   }
