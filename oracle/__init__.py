@@ -12,7 +12,9 @@ loops that follow the per-element definitions of the FlashInfer pages
 compiles it and marshals numpy arrays into it.
 
 Every function here is pinned by ``tests/test_oracle_*.py`` against facts the pages and
-the number formats fix (library casts, brute force, closed forms, invariants).
+the number formats fix (library casts, brute force, closed forms, invariants), except the
+4-token-interleaved V-scale layout (``interleave4_scales`` and the materialize that reads
+it): the pages name that layout without defining it, so its parity is unpinned.
 """
 
 from __future__ import annotations
@@ -112,7 +114,7 @@ def load(path: str):
     L.oracle_materialize_fp8.restype = None
     L.oracle_materialize_fp8.argtypes = (
         [vp, vp, i64, i64, vp, vp, i64, i64, i32, i32, i32, i32, vp, i32, i32, vp,
-         i32, i32, vp, vp, vp, i32, i32])
+         i32, i32, vp, vp, vp, i32, i32, i32])
     L.oracle_kv_quantize.restype = None
     L.oracle_kv_quantize.argtypes = [vp, i32, i64, i64, i64, f32, vp, vp, vp, i32]
     L.oracle_kv_dequantize.restype = None
@@ -272,8 +274,11 @@ def materialize_out_pages(batch_size: int, max_kv_len: int, page_size: int,
 def materialize_fp8(kc: PagedCache, vc: PagedCache, ps: int, H: int, D: int, layout: int,
                     block_tables: np.ndarray, shared: bool, seq_lens, max_kv_len: int,
                     kv_page_indptr, out: np.ndarray, fp8_block_tables: np.ndarray,
-                    zero_tables: bool = True, nthreads: int = 0):
-    """out: uint8 [n_out_pages, 2, H, ps, D]; fp8_block_tables: int32 [B, mpps]."""
+                    zero_tables: bool = True, nthreads: int = 0, v_interleaved4: bool = False):
+    """out: uint8 [n_out_pages, 2, H, ps, D]; fp8_block_tables: int32 [B, mpps].
+    v_interleaved4: vc.sf holds the V scales in the 4-token-interleaved layout (HND only)."""
+    if v_interleaved4 and (layout != 1 or ps % 4 != 0):
+        raise ValueError("4-token-interleaved V scales need HND pages with page_size % 4 == 0")
     bt = np.ascontiguousarray(block_tables, np.int32)
     sl = np.ascontiguousarray(seq_lens, np.int32)
     ip = None if kv_page_indptr is None else np.ascontiguousarray(kv_page_indptr, np.int32)
@@ -282,7 +287,20 @@ def materialize_fp8(kc: PagedCache, vc: PagedCache, ps: int, H: int, D: int, lay
         _p(kc.data), _p(kc.sf), kc.data_page_stride, kc.sf_page_stride,
         _p(vc.data), _p(vc.sf), vc.data_page_stride, vc.sf_page_stride,
         ps, H, D, layout, _p(bt), mnp, int(shared), _p(sl), sl.size, max_kv_len, _p(ip),
-        _p(out), _p(fp8_block_tables), int(zero_tables), nthreads or max_threads())
+        _p(out), _p(fp8_block_tables), int(zero_tables), int(bool(v_interleaved4)),
+        nthreads or max_threads())
+
+
+def interleave4_scales(sf_pages: np.ndarray) -> np.ndarray:
+    """Linear HND block scales [pages, H, page_size, D/16] (uint8) rewritten in the
+    4-token-interleaved layout the materialize parameters name for V: same shape, and within
+    each group of four slots of a head the bytes go block-major, slot-minor (the reading the
+    oracle's materialize follows)."""
+    P, H, ps, nb = sf_pages.shape
+    if ps % 4 != 0:
+        raise ValueError("page_size must be divisible by 4")
+    g = np.ascontiguousarray(sf_pages).reshape(P, H, ps // 4, 4, nb)
+    return np.ascontiguousarray(g.transpose(0, 1, 2, 4, 3)).reshape(P, H, ps, nb)
 
 
 def kv_quantize(x_bits: np.ndarray, is_bf16: bool, gs: float, recipe: Optional[Recipe] = None,

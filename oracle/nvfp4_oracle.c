@@ -37,6 +37,9 @@
  * 4over6 error sum and the reciprocal form of the element scaling x * (1/(S*gs)). The pins
  * fix every result whose rounding decisions are clear of a midpoint and whose candidate
  * errors are not near-tied; the outcomes inside those bands follow the readings alone.
+ * Parity unpinned: the 4-token-interleaved V-scale layout of the materialize input. The
+ * pages name it without defining it; the reading (interleaved4_sf_offset) is pinned only
+ * against a second expression of itself, the layout writer in oracle/__init__.py.
  */
 #include <float.h>
 #include <math.h>
@@ -447,20 +450,35 @@ ORACLE_API void oracle_dequantize_paged(
 /* FP8 materialize ([P3]; [P4] NVFP4KVMaterializer).                                     */
 /* ------------------------------------------------------------------------------------- */
 
+/* Byte offset of V block scale j of (page, head h, slot) when the V scales use the
+ * 4-token-interleaved layout that the materialize parameters name (v_block_scales,
+ * [num_pages, H, page_size, D/16]) without defining it. Reading: the tensor keeps that
+ * shape; within head h's slice of a page the slots go in groups of four (page_size % 4 == 0
+ * is the materializer's requirement), and a group stores block 0 of its four slots, then
+ * block 1, and so on, slot-minor. Parity unpinned: the pages give no example of the
+ * layout. */
+static int64_t interleaved4_sf_offset(int64_t page, int64_t h, int64_t slot, int64_t j,
+                                      int64_t ps, int64_t nb, int64_t sf_page_stride) {
+  int64_t group = slot / 4, lane = slot % 4;
+  return page * sf_page_stride + (h * ps + group * 4) * nb + j * 4 + lane;
+}
+
 /* Output shape [num_pages+1, 2, H, ps, D] float8_e4m3fn. Request b's page j goes to out page
  * o = base_b + j + 1 with base_b = kv_page_indptr[b] (or b * mpps without it); only
  * E2M1 value times E4M3 block scale is applied, rounded to E4M3 (reading: saturating at 448).
  * Page 0 is zero. fp8_block_tables[b, j] = o for the active pages; with zero_tables the other
  * entries are 0 (functional form), otherwise they are left alone (run() form). Reading: every
  * slot of an active page is converted, the copy being page-granular. Reading: a length above
- * mpps*ps is clamped to it. */
+ * mpps*ps is clamped to it. v_sf_layout 1: the V scales are read in the 4-token-interleaved
+ * layout above (HND only; K scales stay linear), 0: linear. */
 ORACLE_API void oracle_materialize_fp8(
     const uint8_t* k_data, const uint8_t* k_sf, int64_t k_data_page_stride,
     int64_t k_sf_page_stride, const uint8_t* v_data, const uint8_t* v_sf,
     int64_t v_data_page_stride, int64_t v_sf_page_stride, int32_t ps, int32_t H, int32_t D,
     int32_t layout, const int32_t* block_tables, int32_t max_num_pages, int32_t shared,
     const int32_t* seq_lens, int32_t B, int32_t max_kv_len, const int32_t* kv_page_indptr,
-    uint8_t* out, int32_t* fp8_block_tables, int32_t zero_tables, int32_t nthreads) {
+    uint8_t* out, int32_t* fp8_block_tables, int32_t zero_tables, int32_t v_sf_layout,
+    int32_t nthreads) {
   int64_t mpps = ((int64_t)max_kv_len + ps - 1) / ps;
   int64_t page_elems = (int64_t)H * ps * D; /* one of K or V of an output page */
   memset(out, 0, (size_t)(2 * page_elems));
@@ -492,7 +510,10 @@ ORACLE_API void oracle_materialize_fp8(
             for (int64_t d = 0; d < D; ++d) {
               uint32_t byte = data[doff + d / 2];
               uint32_t code = (d % 2 == 0) ? (byte & 0xFu) : (byte >> 4);
-              double w = oracle_e2m1_decode(code) * oracle_e4m3_decode(sf[soff + d / 16]);
+              int64_t si = (kv == 1 && v_sf_layout == 1)
+                               ? interleaved4_sf_offset(page, h, slot, d / 16, ps, D / 16, sps)
+                               : soff + d / 16;
+              double w = oracle_e2m1_decode(code) * oracle_e4m3_decode(sf[si]);
               dst[(h * ps + slot) * D + d] = (uint8_t)oracle_e4m3_encode(w);
             }
           }

@@ -648,6 +648,62 @@ def pin_materialize_is_dequant_over_gs(O):
                 assert np.array_equal(got, want), (b, t, kv)
 
 
+def pin_materialize_v_interleaved4(O):
+    """V scales in the 4-token-interleaved layout (the reading: same [pages, H, page_size,
+    D/16] shape; within each head's page slice, groups of four slots, block-major and
+    slot-minor inside a group). (1) The layout writer: marker bytes that name (head, slot,
+    block) land where that description puts them. (2) The materialize that reads them
+    (index arithmetic in C) gives the same copy as the linear form for shared and separate
+    tables, compact and padded pages, while K scales stay linear; reading the interleaved
+    bytes as linear gives another copy, so the check is not vacuous. Parity with the layout
+    itself is unpinned: the pages show no example of it."""
+    H, ps, nb = 2, 8, 4
+    lin = np.zeros((1, H, ps, nb), np.uint8)
+    for h in range(H):
+        for t in range(ps):
+            for j in range(nb):
+                lin[0, h, t, j] = h * 64 + t * 4 + j
+    il = O.interleave4_scales(lin).reshape(H, ps * nb)
+    assert il.shape == (H, ps * nb)
+    for h in range(H):
+        for g in range(ps // 4):
+            group = il[h, g * 4 * nb:(g + 1) * 4 * nb]
+            for run in range(nb):  # a run of four bytes: one block of the group's four slots
+                for lane in range(4):
+                    v = int(group[run * 4 + lane])
+                    assert (v // 64, (v % 64) // 4, v % 4) == (h, g * 4 + lane, run), (h, g, run, lane)
+    one = np.arange(12, dtype=np.uint8).reshape(1, 1, 12, 1)  # one block per slot: identity
+    assert np.array_equal(O.interleave4_scales(one), one)
+
+    rng = np.random.Generator(np.random.PCG64(23))
+    for shared, compact, pad in ((True, False, 0), (False, True, 32)):
+        w = W.random_case(60 + pad, B=4, H=2, D=128, ps=8, layout=W.HND, dtype=torch.bfloat16,
+                          max_len=37, min_len=0, mat_shared=shared, compact_indptr=compact)
+        kc, vc = host_caches(O, w, pad, pad // 8)
+        for c in (kc, vc):
+            c.data[:] = rng.integers(0, 256, c.data.size, dtype=np.uint8)
+            sfb = rng.integers(0, 256, c.sf.size, dtype=np.uint8)
+            sfb[(sfb & 0x7F) == 0x7F] = 0x7E
+            c.sf[:] = sfb
+        sv = vc.sf.reshape(w.num_pages, vc.sf_page_stride)
+        body = w.H * w.ps * (w.D // 16)
+        vil = O.PagedCache(vc.data, vc.sf.copy(), vc.data_page_stride, vc.sf_page_stride)
+        vil.sf.reshape(w.num_pages, vc.sf_page_stride)[:, :body] = O.interleave4_scales(
+            sv[:, :body].reshape(w.num_pages, w.H, w.ps, w.D // 16)).reshape(w.num_pages, body)
+        n_out, mpps = O.materialize_out_pages(w.B, w.max_kv_len, w.ps, w.mat_num_pages)
+        outs = []
+        for vcache, flag in ((vc, False), (vil, True), (vil, False)):
+            out = np.zeros((n_out, 2, w.H, w.ps, w.D), np.uint8)
+            tbl = np.zeros((w.B, mpps), np.int32)
+            O.materialize_fp8(kc, vcache, w.ps, w.H, w.D, W.HND, w.mat_block_tables, shared,
+                              w.seq_lens, w.max_kv_len, w.kv_page_indptr, out, tbl, True, 2,
+                              v_interleaved4=flag)
+            outs.append(out)
+        assert np.array_equal(outs[0], outs[1]), (shared, compact, pad)
+        assert np.array_equal(outs[0][:, 0], outs[2][:, 0])
+        assert not np.array_equal(outs[0][:, 1], outs[2][:, 1])
+
+
 def pin_exact_tie_keeps_amax6(O):
     """A block that both candidates reconstruct exactly (constant magnitude c with c/6 and
     c/4 both E4M3 values) ties at zero error; the tie keeps the amax/6 scale."""
@@ -808,7 +864,8 @@ ALL_PINS = [
     pin_e2m1_decode, pin_e2m1_encode, pin_e4m3_decode, pin_e4m3_encode, pin_f16, pin_bf16,
     pin_global_scale, pin_roundtrip, pin_block_vs_exact, pin_4over6_behaviour,
     pin_recipe_mismatch, pin_append_addressing, pin_dequant, pin_materialize,
-    pin_materialize_is_dequant_over_gs, pin_exact_tie_keeps_amax6,
+    pin_materialize_is_dequant_over_gs, pin_materialize_v_interleaved4,
+    pin_exact_tie_keeps_amax6,
     pin_fast_math_differs_only_near_ties, pin_dequant_multiplication_order,
     pin_kv_quantize, pin_kv_dequantize,
 ]

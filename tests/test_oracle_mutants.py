@@ -47,6 +47,14 @@ MUTANTS = {
     "global_scale_ignores_recipe": (
         "float denom = 6.0f * oracle_e4m3_max(r);", "float denom = 6.0f * 448.0f;"),
     "global_scale_zero_tensor": ("if (amax == 0.0f) return 1.0f;", ""),
+    "v_interleave_read_as_linear": (
+        "return page * sf_page_stride + (h * ps + group * 4) * nb + j * 4 + lane;",
+        "return page * sf_page_stride + (h * ps + group * 4 + lane) * nb + j;"),
+    "v_interleave_applied_to_k": (
+        "int64_t si = (kv == 1 && v_sf_layout == 1)", "int64_t si = (v_sf_layout == 1)"),
+    "v_interleave_groups_span_heads": (
+        "return page * sf_page_stride + (h * ps + group * 4) * nb + j * 4 + lane;",
+        "return page * sf_page_stride + (group * 4 * 2 + h * 4) * nb + j * 4 + lane;"),
     "hnd_addressed_as_nhd": (
         "return layout == 0 ? slot * H + h : h * ps + slot;", "return slot * H + h;"),
     "append_slot_off_by_one": ("int64_t slot = pos % ps;", "int64_t slot = (pos + 1) % ps;"),
@@ -81,7 +89,7 @@ MUTANTS = {
         "dequant_value(code, sf[i * (cols / 16) + d / 16], gs, out_bf16);",
         "dequant_value(code, sf[i * (cols / 16) + ((d / 16) + 1) % (cols / 16)], gs, out_bf16);"),
     "materialize_applies_nothing": (
-        "double w = oracle_e2m1_decode(code) * oracle_e4m3_decode(sf[soff + d / 16]);",
+        "double w = oracle_e2m1_decode(code) * oracle_e4m3_decode(sf[si]);",
         "double w = oracle_e2m1_decode(code);"),
 }
 
