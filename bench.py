@@ -205,13 +205,18 @@ class ClockSampler:
 class Step:
     """Buffers and launches of one pass of the hot path on the current device."""
 
-    def __init__(self, w: W.Workload, dev: torch.device):
+    def __init__(self, w: W.Workload, dev: torch.device, v_scales: str = "linear"):
         import nvfp4_paged_kv_02_gb300 as nv
         self.nv, self.w, self.dev = nv, w, dev
         r = w.recipe
         self.recipe = None if r is None else nv.NVFP44Over6Config(
             r.e4m3_max, "MSE" if r.err_mode else "MAE", bool(r.err_use_fast_math))
         t = lambda a: torch.as_tensor(np.ascontiguousarray(a)).to(dev)
+        if v_scales not in ("linear", "interleaved4"):
+            raise ValueError(v_scales)
+        if v_scales == "interleaved4" and w.layout != W.HND:
+            raise SystemExit("4-token-interleaved V scales need an HND workload")
+        self.v_scales = v_scales
         inner = (w.ps, w.H) if w.layout == W.NHD else (w.H, w.ps)
         self.cache = tuple(torch.empty((w.num_pages, *inner, w.D // 2), dtype=torch.uint8,
                                        device=dev) for _ in range(2))
@@ -245,6 +250,15 @@ class Step:
                 float(self.gv.item()), self.lay, self.recipe, self.status)
             del pk, pv
 
+        self.mat_v_sf = self.sf[1]
+        if v_scales == "interleaved4":
+            # The measured append writes the same bytes at every step. Its V scales, rewritten
+            # once in the 4-token-interleaved layout, are what the materialize then reads.
+            self._global_scales()
+            self._append()
+            P, Hh, ps, nb = self.sf[1].shape
+            self.mat_v_sf = self.sf[1].view(P, Hh, ps // 4, 4, nb).transpose(3, 4) \
+                .contiguous().view(P, Hh, ps, nb)
         self._ops = [self._global_scales, self._append, self._dequant, self._materialize]
 
     NAMES = ("global_scale", "append", "dequant_paged", "materialize")
@@ -266,9 +280,9 @@ class Step:
     def _materialize(self):
         w = self.w
         self.nv.nvfp4_materialize_fp8(
-            self.cache[0], self.cache[1], self.sf[0], self.sf[1], self.mat_bt, self.seq_lens,
+            self.cache[0], self.cache[1], self.sf[0], self.mat_v_sf, self.mat_bt, self.seq_lens,
             w.max_kv_len, w.mat_shared, self.fp8, self.indptr, w.mat_num_pages, self.lay,
-            self.tables, True, self.status)
+            self.tables, True, self.status, v_block_scales_layout=self.v_scales)
 
     def run(self, ev=None, flush=None):
         run_ops(self._ops, ev, flush)
@@ -283,7 +297,8 @@ class Step:
                 "kv_layout": "NHD" if w.layout == W.NHD else "HND",
                 "input_dtype": str(w.dtype).replace("torch.", ""),
                 "recipe": None if w.recipe is None else vars(w.recipe),
-                "pool_pages": w.num_pages, "active_pages": active_pages(w)}
+                "pool_pages": w.num_pages, "active_pages": active_pages(w),
+                "materialize_v_scales": self.v_scales}
 
 
 def run_ops(ops, ev=None, flush=None):
@@ -514,6 +529,8 @@ def main():
                     help="large_pool: pool size (K+V codes and scales), GB")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--v-scales", default="linear", choices=["linear", "interleaved4"],
+                    help="layout of the V block scales the materialize reads (HND workloads)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -540,7 +557,7 @@ def main():
     import nvfp4_paged_kv_02_gb300 as nv
     nv.load()
     w = make_workload(args.workload, dev, args.batch, args.pool_gb)
-    step = ContigStep(w, dev) if args.workload == "contig" else Step(w, dev)
+    step = ContigStep(w, dev) if args.workload == "contig" else Step(w, dev, args.v_scales)
     nbytes, ntok = step.op_bytes()
     n_ops = len(step.NAMES)
     total_bytes = sum(nbytes.values())

@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define NVFP4KV_ABI_VERSION 1
+#define NVFP4KV_ABI_VERSION 2
 
 /* Return codes. */
 typedef int32_t nvfp4_status;
@@ -70,6 +70,15 @@ typedef int32_t nvfp4_status;
 /* Integer type of a dequantize block table. */
 #define NVFP4_I32 0
 #define NVFP4_I64 1
+
+/* Layouts of a materialize V block-scale cache. LINEAR: [pages, H, page_size, D/16] row
+ * after row (the K layout). INTERLEAVED4: the "4-token-interleaved" layout the materialize
+ * parameters name for v_block_scales without defining it; this library's reading keeps the
+ * shape and, within each head's page slice, stores each group of four slots block-major and
+ * slot-minor: block j of slot t of head h sits at byte
+ * (h * page_size + (t & ~3)) * (D/16) + 4 j + (t & 3) of the page. */
+#define NVFP4_SF_LINEAR 0
+#define NVFP4_SF_INTERLEAVED4 1
 
 /* 4over6 error metrics ("NVFP44Over6ErrMode"): summed absolute or summed squared error. */
 #define NVFP4_ERR_MAE 0
@@ -241,15 +250,17 @@ nvfp4_status nvfp4_materialize_fp8_out_pages(int32_t batch_size, int32_t max_kv_
  *   zero_fp8_block_tables  1: entries past each request's pages are set to 0 (the
  *                  functional API's padding); 0: they are left alone (run(), where the
  *                  caller zeroes the table once per step).
+ *   v_scale_layout NVFP4_SF_LINEAR, or NVFP4_SF_INTERLEAVED4 for V scales in the
+ *                  4-token-interleaved layout (HND only; K scales are always linear).
  * Requirements (the materializer's): head_dim % 64 == 0, page_size % 4 == 0. Layout HND
- * is the pages' input layout; NHD input is also accepted. */
+ * is the pages' input layout; NHD input is also accepted with linear scales. */
 nvfp4_status nvfp4_materialize_fp8(
     nvfp4_paged_cache k_cache, nvfp4_paged_cache v_cache, int32_t page_size,
     int32_t num_kv_heads, int32_t head_dim, int32_t kv_layout, const int32_t* block_tables,
     int32_t max_num_pages, int32_t uses_shared_paged_kv_idx, const int32_t* seq_lens,
     int32_t batch_size, int32_t max_kv_len, const int32_t* kv_page_indptr, int64_t num_pages,
     uint8_t* out, int64_t out_num_pages, int32_t* fp8_block_tables,
-    int32_t zero_fp8_block_tables, int32_t* dev_status, void* stream);
+    int32_t zero_fp8_block_tables, int32_t v_scale_layout, int32_t* dev_status, void* stream);
 
 /* Quantize a contiguous fp16/bf16 tensor to NVFP4 with linear block scales
  * ("flashinfer.quantization" index, "FP4 KV Cache Quantization": nvfp4_kv_quantize).

@@ -39,6 +39,7 @@ LIB_PATH = _build.LIB_PATH
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_CUDA = 0, 1, 2, 3, 4
 F16, BF16 = 0, 1
 NHD, HND = 0, 1
+SF_LINEAR, SF_INTERLEAVED4 = 0, 1  # materialize V block-scale layouts
 I32, I64 = 0, 1
 DEV_BAD_BATCH, DEV_BAD_POSITION, DEV_BAD_PAGE, DEV_LEN_CLAMPED, DEV_BAD_OUT_PAGE = 1, 2, 4, 8, 16
 DEV_TIMEOUT, DEV_BAD_SCALE = 32, 64
@@ -110,7 +111,7 @@ def load() -> ctypes.CDLL:
         L.nvfp4_materialize_fp8.restype = i32
         L.nvfp4_materialize_fp8.argtypes = [
             _Cache, _Cache, i32, i32, i32, i32, vp, i32, i32, vp, i32, i32, vp, i64, vp, i64, vp,
-            i32, vp, vp]
+            i32, i32, vp, vp]
         L.nvfp4_4over6_code.restype = i32
         L.nvfp4_4over6_code.argtypes = [vp, vp]
         L.nvfp4_4over6_from_code.restype = i32
@@ -145,6 +146,13 @@ def _layout(kv_layout: Union[str, int]) -> int:
     if isinstance(kv_layout, int):
         return kv_layout
     return {"NHD": NHD, "HND": HND}[kv_layout.upper()]
+
+
+def _sf_layout(v_block_scales_layout: Union[str, int]) -> int:
+    """'linear' or 'interleaved4' (the 4-token-interleaved V-scale layout, HND only)."""
+    if isinstance(v_block_scales_layout, int):
+        return v_block_scales_layout
+    return {"linear": SF_LINEAR, "interleaved4": SF_INTERLEAVED4}[v_block_scales_layout.lower()]
 
 
 def _dtype_code(dt: torch.dtype) -> int:
@@ -321,10 +329,12 @@ def nvfp4_materialize_fp8(k_cache: torch.Tensor, v_cache: torch.Tensor,
                           num_pages: Optional[int] = None, kv_layout: str = "HND",
                           fp8_block_tables: Optional[torch.Tensor] = None,
                           zero_fp8_block_tables: bool = True,
-                          dev_status: Optional[torch.Tensor] = None):
+                          dev_status: Optional[torch.Tensor] = None,
+                          v_block_scales_layout: str = "linear"):
     """Materialize the active pages as FP8 E4M3. Returns (kv_cache_fp8, fp8_block_tables)
     with kv_cache_fp8 [num_pages + 1, 2, H, page_size, D] (page 0 zero) and
-    fp8_block_tables [batch, max_pages_per_seq] int32 (padding 0)."""
+    fp8_block_tables [batch, max_pages_per_seq] int32 (padding 0). v_block_scales_layout
+    'interleaved4' reads the V scales in the 4-token-interleaved layout (HND pages)."""
     layout = _layout(kv_layout)
     kc = _one_cache(k_cache, k_block_scales)
     vc = _one_cache(v_cache, v_block_scales)
@@ -352,8 +362,8 @@ def nvfp4_materialize_fp8(k_cache: torch.Tensor, v_cache: torch.Tensor,
         kc._c(), vc._c(), ps, H, D, layout, _ptr(block_tables), block_tables.shape[-1],
         int(shared), _ptr(seq_lens), B, int(max_kv_len), _ptr(kv_page_indptr),
         -1 if num_pages is None else int(num_pages), _ptr(out), out.shape[0],
-        _ptr(fp8_block_tables), int(bool(zero_fp8_block_tables)), _ptr(dev_status),
-        _stream(dev)))
+        _ptr(fp8_block_tables), int(bool(zero_fp8_block_tables)),
+        _sf_layout(v_block_scales_layout), _ptr(dev_status), _stream(dev)))
     return out, fp8_block_tables
 
 
@@ -366,7 +376,8 @@ class NVFP4KVMaterializer:
 
     def __init__(self, num_kv_heads: int, page_size: int, head_dim: int,
                  device: Union[str, int, torch.device] = "cuda",
-                 uses_shared_paged_kv_idx: bool = True, kv_layout: str = "HND"):
+                 uses_shared_paged_kv_idx: bool = True, kv_layout: str = "HND",
+                 v_block_scales_layout: str = "linear"):
         if page_size % 4 != 0:
             raise ValueError("page_size must be divisible by 4")
         if head_dim % 64 != 0:
@@ -377,6 +388,9 @@ class NVFP4KVMaterializer:
             raise ValueError("NVFP4KVMaterializer needs a CUDA device")
         self.shared = bool(uses_shared_paged_kv_idx)
         self.layout = _layout(kv_layout)
+        self.v_sf_layout = _sf_layout(v_block_scales_layout)
+        if self.v_sf_layout == SF_INTERLEAVED4 and self.layout != HND:
+            raise ValueError("4-token-interleaved V scales need HND pages")
         self._lib = load()
 
     def run(self, k_cache, v_cache, k_block_scales, v_block_scales, block_tables, seq_lens,
@@ -389,7 +403,8 @@ class NVFP4KVMaterializer:
             kc._c(), vc._c(), self.ps, self.H, self.D, self.layout, _ptr(block_tables),
             block_tables.shape[-1], int(self.shared), _ptr(seq_lens), B, mpps * self.ps,
             _ptr(kv_page_indptr), out.shape[0] - 1, _ptr(out), out.shape[0],
-            _ptr(fp8_block_tables), 0, _ptr(dev_status), _stream(self.device)))
+            _ptr(fp8_block_tables), 0, self.v_sf_layout, _ptr(dev_status),
+            _stream(self.device)))
         return out, fp8_block_tables
 
 

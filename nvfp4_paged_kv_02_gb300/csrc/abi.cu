@@ -462,9 +462,11 @@ NVFP4_EXPORT nvfp4_status nvfp4_materialize_fp8(
     int32_t max_num_pages, int32_t uses_shared_paged_kv_idx, const int32_t* seq_lens,
     int32_t batch_size, int32_t max_kv_len, const int32_t* kv_page_indptr, int64_t num_pages,
     uint8_t* out, int64_t out_num_pages, int32_t* fp8_block_tables,
-    int32_t zero_fp8_block_tables, int32_t* dev_status, void* stream) {
+    int32_t zero_fp8_block_tables, int32_t v_scale_layout, int32_t* dev_status, void* stream) {
   clear_error();
   const char* fn = "nvfp4_materialize_fp8";
+  if (v_scale_layout != NVFP4_SF_LINEAR && v_scale_layout != NVFP4_SF_INTERLEAVED4)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materialize_fp8: v_scale_layout must be NVFP4_SF_LINEAR or NVFP4_SF_INTERLEAVED4");
   if (nvfp4_status st = check_geometry(fn, page_size, num_kv_heads, head_dim, kv_layout)) return st;
   if (head_dim % 64 != 0) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materialize_fp8: head_dim must be divisible by 64");
   if (page_size % 4 != 0) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materialize_fp8: page_size must be divisible by 4");
@@ -472,6 +474,8 @@ NVFP4_EXPORT nvfp4_status nvfp4_materialize_fp8(
     return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materialize_fp8: negative size");
   if (nvfp4_status st = check_cache(fn, "k_cache", k_cache, page_size, num_kv_heads, head_dim)) return st;
   if (nvfp4_status st = check_cache(fn, "v_cache", v_cache, page_size, num_kv_heads, head_dim)) return st;
+  if (v_scale_layout == NVFP4_SF_INTERLEAVED4 && kv_layout != NVFP4_HND)
+    return fail(NVFP4_ERR_UNSUPPORTED, "nvfp4_materialize_fp8: 4-token-interleaved V scales are defined for HND pages only");
   if (!aligned(k_cache.sf, 2) || !aligned(v_cache.sf, 2) || k_cache.sf_page_stride % 2 != 0 ||
       v_cache.sf_page_stride % 2 != 0)
     return fail(NVFP4_ERR_ALIGNMENT, "nvfp4_materialize_fp8: scale caches must be 2-byte aligned with even page strides");
@@ -514,6 +518,7 @@ NVFP4_EXPORT nvfp4_status nvfp4_materialize_fp8(
   a.out_num_pages = out_num_pages;
   a.tables = fp8_block_tables;
   a.zero_tables = zero_fp8_block_tables ? 1 : 0;
+  a.v_interleaved = v_scale_layout == NVFP4_SF_INTERLEAVED4 ? 1 : 0;
   a.pipe = pipe_test_from_env();
   a.status = dev_status;
   if (batch_size == 0) {

@@ -114,6 +114,7 @@ struct MaterializeArgs {
   int64_t out_num_pages;
   int32_t* tables;
   int32_t zero_tables;
+  int32_t v_interleaved;  // V scales in the 4-token-interleaved layout (HND pages)
   PipeTest pipe;
   int32_t* status;
 };

@@ -12,6 +12,13 @@
 // 32-element chunk k of the output half page (16 code bytes + 2 scale bytes in, one
 // 32-byte store out). With HND input, chunk k is also the k-th 16-byte chunk of the input
 // page, so both streams are contiguous.
+//
+// V scales may also come in the 4-token-interleaved layout the materialize parameters name
+// for v_block_scales (HND only). The pages do not define it; the reading taken here keeps
+// the [pages, H, page_size, D/16] shape and, within each head's page slice, stores each
+// group of four slots block-major and slot-minor, so block j of page row r (= h * ps + slot)
+// is byte (r & ~3) * (D/16) + 4 j + (r & 3). Only the scale index changes: the page is
+// still one contiguous run of scale bytes.
 #include "internal.h"
 #include "pipeline.cuh"
 #include "scan.cuh"
@@ -51,6 +58,18 @@ __device__ __forceinline__ U32x8 convert_chunk(uint4 c, uint32_t s01) {
   return o;
 }
 
+// The two scale bytes of output chunk k (blocks 2c and 2c + 1 of page row r = k / (D/32)).
+// Linear: the 16-bit word at chunk offset `off`. Interleaved V (HND, so off == k): bytes
+// (r & ~3) * (D/16) + 8c + (r & 3) and 4 bytes after it.
+__device__ __forceinline__ uint32_t interleaved4_scales(const uint8_t* sf, int32_t k,
+                                                        int32_t row_chunks, Div div_row_chunks) {
+  const int32_t r = static_cast<int32_t>(div_q(k, div_row_chunks));
+  const int32_t c = k - r * row_chunks;
+  const int32_t i0 = (r & ~3) * (2 * row_chunks) + 8 * c + (r & 3);
+  return static_cast<uint32_t>(sf[i0]) | (static_cast<uint32_t>(sf[i0 + 4]) << 8);
+}
+
+template <bool VIL>
 __global__ void __launch_bounds__(kThreads) materialize_kernel(const MaterializeArgs a) {
   extern __shared__ int32_t s_cum[];
   const int32_t ps = a.ps;
@@ -129,7 +148,10 @@ __global__ void __launch_bounds__(kThreads) materialize_kernel(const Materialize
             off = (slot * a.H + h) * row_chunks + (rem - slot * row_chunks);
           }
           cv[u] = __ldg(reinterpret_cast<const uint4*>(pd) + off);
-          sv[u] = __ldg(reinterpret_cast<const uint16_t*>(psf) + off);
+          if (VIL && kv)
+            sv[u] = interleaved4_scales(psf, k, row_chunks, a.div_row_chunks);
+          else
+            sv[u] = __ldg(reinterpret_cast<const uint16_t*>(psf) + off);
         }
       }
 #pragma unroll
@@ -147,6 +169,7 @@ __global__ void __launch_bounds__(kThreads) materialize_kernel(const Materialize
 // and bulk-copies the source page's codes and scales into the next free shared-memory
 // stage; the consumer warps convert from shared memory and stream the 32-byte stores.
 
+template <bool VIL>
 __global__ void __launch_bounds__(kTmaThreads, 3) materialize_tma_kernel(const MaterializeArgs a,
                                                                        const TmaLayout L) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -273,18 +296,27 @@ __global__ void __launch_bounds__(kTmaThreads, 3) materialize_tma_kernel(const M
         const uint8_t* st = stages + static_cast<uint32_t>(s) * L.stage_bytes;
         const uint8_t* sfp = st + L.sf_off;
         uint8_t* dst = a.out + (static_cast<int64_t>(m.f0) * 2 + m.f1) * half_page;
+        if (VIL && m.f1) {  // interleaved V scales (HND pages only)
 #pragma unroll 4
-        for (int32_t k = ct; k < chunks; k += kConsumers) {
-          int32_t off = k;  // HND: chunk k of the output is chunk k of the input page
-          if (a.layout == NVFP4_NHD) {
-            const int32_t h = static_cast<int32_t>(div_q(k, a.div_page_chunks));
-            const int32_t rem = k - h * (ps * row_chunks);
-            const int32_t slot = static_cast<int32_t>(div_q(rem, a.div_row_chunks));
-            off = (slot * a.H + h) * row_chunks + (rem - slot * row_chunks);
+          for (int32_t k = ct; k < chunks; k += kConsumers) {
+            const uint4 c = *reinterpret_cast<const uint4*>(st + 16 * k);
+            const uint32_t s01 = interleaved4_scales(sfp, k, row_chunks, a.div_row_chunks);
+            st_256(dst + static_cast<int64_t>(k) * 32, convert_chunk(c, s01));
           }
-          const uint4 c = *reinterpret_cast<const uint4*>(st + 16 * off);
-          const uint32_t s01 = *reinterpret_cast<const uint16_t*>(sfp + 2 * off);
-          st_256(dst + static_cast<int64_t>(k) * 32, convert_chunk(c, s01));
+        } else {
+#pragma unroll 4
+          for (int32_t k = ct; k < chunks; k += kConsumers) {
+            int32_t off = k;  // HND: chunk k of the output is chunk k of the input page
+            if (a.layout == NVFP4_NHD) {
+              const int32_t h = static_cast<int32_t>(div_q(k, a.div_page_chunks));
+              const int32_t rem = k - h * (ps * row_chunks);
+              const int32_t slot = static_cast<int32_t>(div_q(rem, a.div_row_chunks));
+              off = (slot * a.H + h) * row_chunks + (rem - slot * row_chunks);
+            }
+            const uint4 c = *reinterpret_cast<const uint4*>(st + 16 * off);
+            const uint32_t s01 = *reinterpret_cast<const uint16_t*>(sfp + 2 * off);
+            st_256(dst + static_cast<int64_t>(k) * 32, convert_chunk(c, s01));
+          }
         }
       }
       __syncwarp();
@@ -304,7 +336,7 @@ nvfp4_status launch_materialize(const MaterializeArgs& a, cudaStream_t stream) {
   const int64_t cb = static_cast<int64_t>(a.ps) * a.H * (a.D / 2);
   const int64_t sb = static_cast<int64_t>(a.ps) * a.H * (a.D / 16);
   if (pages_bulk_copyable(a.kc, a.vc, cb, sb)) {
-    const auto kern = materialize_tma_kernel;
+    const auto kern = a.v_interleaved ? materialize_tma_kernel<true> : materialize_tma_kernel<false>;
     const TmaLayout L = tma_layout(a.B, static_cast<uint32_t>(cb), static_cast<uint32_t>(sb),
                                    stages_for(static_cast<uint32_t>(cb), static_cast<uint32_t>(sb)));
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -314,7 +346,7 @@ nvfp4_status launch_materialize(const MaterializeArgs& a, cudaStream_t stream) {
     kern<<<grid, kTmaThreads, L.total, stream>>>(a, L);
     return check_launch("nvfp4_materialize_fp8");
   }
-  const auto kern = materialize_kernel;
+  const auto kern = a.v_interleaved ? materialize_kernel<true> : materialize_kernel<false>;
   const size_t smem = static_cast<size_t>(a.B) * sizeof(int32_t);
   if (smem > 48 * 1024) {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_e4m3_max(lib):
-    assert lib.nvfp4_abi_version() == 1
+    assert lib.nvfp4_abi_version() == 2
     assert nv.nvfp4_e4m3_max(None) == 448.0
     assert nv.nvfp4_e4m3_max(nv.NVFP44Over6Config(256.0, "MSE")) == 256.0
 
@@ -148,13 +148,13 @@ def test_empty_dequant_is_a_no_op(lib):
 
 def materialize(lib, **kw):
     a = dict(kc=cache(), vc=cache(), ps=16, H=8, D=128, layout=1, mnp=4, shared=1, B=2, mkl=64,
-             indptr=None, npages=-1, out=FAKE, nout=9)
+             indptr=None, npages=-1, out=FAKE, nout=9, vsf=nv.SF_LINEAR)
     a.update(kw)
     return lib.nvfp4_materialize_fp8(
         a["kc"], a["vc"], a["ps"], a["H"], a["D"], a["layout"], ctypes.c_void_p(FAKE), a["mnp"],
         a["shared"], ctypes.c_void_p(FAKE), a["B"], a["mkl"],
         None if a["indptr"] is None else ctypes.c_void_p(a["indptr"]), a["npages"],
-        ctypes.c_void_p(a["out"]), a["nout"], ctypes.c_void_p(FAKE), 1, None, None)
+        ctypes.c_void_p(a["out"]), a["nout"], ctypes.c_void_p(FAKE), 1, a["vsf"], None, None)
 
 
 @pytest.mark.parametrize("kw,code,text", [
@@ -165,10 +165,20 @@ def materialize(lib, **kw):
     (dict(indptr=FAKE), nv.ERR_INVALID_ARG, "requires num_pages"),
     (dict(indptr=FAKE, npages=20, nout=20), nv.ERR_INVALID_ARG, "num_pages + 1"),
     (dict(out=FAKE + 16), nv.ERR_ALIGNMENT, "32-byte"),
+    (dict(vsf=2), nv.ERR_INVALID_ARG, "v_scale_layout"),
+    (dict(vsf=nv.SF_INTERLEAVED4, layout=0), nv.ERR_UNSUPPORTED, "HND pages only"),
 ])
 def test_materialize_rejects(lib, kw, code, text):
     assert materialize(lib, **kw) == code
     assert text in err(lib)
+
+
+def test_materializer_interleaved_needs_hnd():
+    with pytest.raises(ValueError, match="HND"):
+        nv.NVFP4KVMaterializer(8, 16, 128, "cuda", kv_layout="NHD",
+                               v_block_scales_layout="interleaved4")
+    with pytest.raises(KeyError):
+        nv.NVFP4KVMaterializer(8, 16, 128, "cuda", v_block_scales_layout="swizzled")
 
 
 def test_global_scale_rejects(lib):
