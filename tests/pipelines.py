@@ -210,3 +210,72 @@ def assert_same(a: Result, b: Result, what: str = ""):
         assert bad.size == 0, (f"{what}: {name} differs at {bad.size} of {x.size} positions; "
                                f"first {bad[:8].tolist()} gpu={x.reshape(-1)[bad[:8]].tolist()} "
                                f"oracle={y.reshape(-1)[bad[:8]].tolist()}")
+
+
+# ---- materialize with V scales in the 4-token-interleaved layout ---------------------------
+
+def interleaved_v(w: W.Workload, vc: O.PagedCache) -> O.PagedCache:
+    """A copy of an HND host cache whose V scale pages are rewritten by the oracle's layout
+    writer (the codes are shared)."""
+    body = w.H * w.ps * (w.D // 16)
+    sf = vc.sf.copy()
+    pages = sf.reshape(w.num_pages, vc.sf_page_stride)
+    pages[:, :body] = O.interleave4_scales(
+        pages[:, :body].reshape(w.num_pages, w.H, w.ps, w.D // 16)).reshape(w.num_pages, body)
+    return O.PagedCache(vc.data, sf, vc.data_page_stride, vc.sf_page_stride)
+
+
+def hnd_views(w: W.Workload, c: O.PagedCache, dev):
+    """The documented HND 4-D device views [pages, H, page_size, D/2 | D/16] of a host cache,
+    with its page strides."""
+    bd = torch.from_numpy(c.data.copy()).to(dev).view(w.num_pages, c.data_page_stride)
+    bs = torch.from_numpy(c.sf.copy()).to(dev).view(w.num_pages, c.sf_page_stride)
+    d = bd[:, : w.H * w.ps * w.D // 2].unflatten(1, (w.H, w.ps, w.D // 2))
+    s = bs[:, : w.H * w.ps * w.D // 16].unflatten(1, (w.H, w.ps, w.D // 16))
+    return d, s
+
+
+@dataclass
+class InterleavedResult:
+    got: np.ndarray
+    want: np.ndarray
+    got_tables: np.ndarray
+    want_tables: np.ndarray
+    status: int
+
+
+def run_materialize_interleaved(w: W.Workload, kc: O.PagedCache, vc: O.PagedCache,
+                                extra_out_pages: int = 0, zero_tables: bool = True,
+                                use_class: bool = False, device="cuda") -> InterleavedResult:
+    """FP8 materialize of one HND host cache pair whose V scales are rewritten in the
+    4-token-interleaved layout: the oracle and the CUDA library read the same bytes."""
+    import nvfp4_paged_kv_02_gb300 as nv
+    dev = torch.device(device)
+    vil = interleaved_v(w, vc)
+    n_out, mpps = mat_shape(w)
+    n_out += extra_out_pages
+    want = np.full((n_out, 2, w.H, w.ps, w.D), SENT_FP8, np.uint8)
+    want_tbl = np.full((w.B, mpps), SENT_TABLE, np.int32)
+    O.materialize_fp8(kc, vil, w.ps, w.H, w.D, W.HND, w.mat_block_tables, w.mat_shared,
+                      w.seq_lens, w.max_kv_len, w.kv_page_indptr, want, want_tbl, zero_tables,
+                      v_interleaved4=True)
+    kd, ks = hnd_views(w, kc, dev)
+    vd, vs = hnd_views(w, vil, dev)
+    t = lambda a: torch.as_tensor(np.ascontiguousarray(a)).to(dev)
+    out = torch.full((n_out, 2, w.H, w.ps, w.D), SENT_FP8, dtype=torch.uint8,
+                     device=dev).view(torch.float8_e4m3fn)
+    tbl = torch.full((w.B, mpps), SENT_TABLE, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    indptr = None if w.kv_page_indptr is None else t(w.kv_page_indptr)
+    if use_class:
+        m = nv.NVFP4KVMaterializer(w.H, w.ps, w.D, dev, uses_shared_paged_kv_idx=w.mat_shared,
+                                   v_block_scales_layout="interleaved4")
+        m.run(kd, vd, ks, vs, t(w.mat_block_tables), t(w.seq_lens), indptr, out=out,
+              fp8_block_tables=tbl, dev_status=status)
+    else:
+        nv.nvfp4_materialize_fp8(kd, vd, ks, vs, t(w.mat_block_tables), t(w.seq_lens),
+                                 w.max_kv_len, w.mat_shared, out, indptr, w.mat_num_pages, "HND",
+                                 tbl, zero_tables, status, v_block_scales_layout="interleaved4")
+    torch.cuda.synchronize(dev)
+    return InterleavedResult(out.view(torch.uint8).cpu().numpy(), want, tbl.cpu().numpy(),
+                             want_tbl, int(status.item()))

@@ -27,15 +27,6 @@ def _cuda(gpu_lib):
     yield
 
 
-def _interleaved_v(w: W.Workload, vc: O.PagedCache) -> O.PagedCache:
-    body = w.H * w.ps * (w.D // 16)
-    sf = vc.sf.copy()
-    pages = sf.reshape(w.num_pages, vc.sf_page_stride)
-    pages[:, :body] = O.interleave4_scales(
-        pages[:, :body].reshape(w.num_pages, w.H, w.ps, w.D // 16)).reshape(w.num_pages, body)
-    return O.PagedCache(vc.data, sf, vc.data_page_stride, vc.sf_page_stride)
-
-
 def _random_caches(w: W.Workload, pad_data: int, pad_sf: int, seed: int):
     rng = np.random.Generator(np.random.PCG64(seed))
     dps, sps = PL.strides(w, pad_data, pad_sf)
@@ -48,51 +39,14 @@ def _random_caches(w: W.Workload, pad_data: int, pad_sf: int, seed: int):
     return out
 
 
-def _to_dev(w: W.Workload, c: O.PagedCache, dev):
-    """The documented HND 4-D views [pages, H, page_size, D/2 | D/16] of a host cache."""
-    bd = torch.from_numpy(c.data.copy()).to(dev).view(w.num_pages, c.data_page_stride)
-    bs = torch.from_numpy(c.sf.copy()).to(dev).view(w.num_pages, c.sf_page_stride)
-    d = bd[:, : w.H * w.ps * w.D // 2].unflatten(1, (w.H, w.ps, w.D // 2))
-    s = bs[:, : w.H * w.ps * w.D // 16].unflatten(1, (w.H, w.ps, w.D // 16))
-    return d, s
-
-
 def _compare(w: W.Workload, kc, vc, extra_out_pages=0, zero_tables=True, use_class=False):
     import nvfp4_paged_kv_02_gb300 as nv
-    dev = torch.device("cuda")
-    vil = _interleaved_v(w, vc)
-    n_out, mpps = PL.mat_shape(w)
-    n_out += extra_out_pages
-    want = np.full((n_out, 2, w.H, w.ps, w.D), PL.SENT_FP8, np.uint8)
-    want_tbl = np.full((w.B, mpps), PL.SENT_TABLE, np.int32)
-    O.materialize_fp8(kc, vil, w.ps, w.H, w.D, W.HND, w.mat_block_tables, w.mat_shared,
-                      w.seq_lens, w.max_kv_len, w.kv_page_indptr, want, want_tbl, zero_tables,
-                      v_interleaved4=True)
-    kd, ks = _to_dev(w, kc, dev)
-    vd, vs = _to_dev(w, vil, dev)
-    t = lambda a: torch.as_tensor(np.ascontiguousarray(a)).to(dev)
-    out = torch.full((n_out, 2, w.H, w.ps, w.D), PL.SENT_FP8, dtype=torch.uint8,
-                     device=dev).view(torch.float8_e4m3fn)
-    tbl = torch.full((w.B, mpps), PL.SENT_TABLE, dtype=torch.int32, device=dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    indptr = None if w.kv_page_indptr is None else t(w.kv_page_indptr)
-    if use_class:
-        m = nv.NVFP4KVMaterializer(w.H, w.ps, w.D, dev, uses_shared_paged_kv_idx=w.mat_shared,
-                                   v_block_scales_layout="interleaved4")
-        m.run(kd, vd, ks, vs, t(w.mat_block_tables), t(w.seq_lens),
-              indptr if indptr is not None else None, out=out, fp8_block_tables=tbl,
-              dev_status=status)
-    else:
-        nv.nvfp4_materialize_fp8(kd, vd, ks, vs, t(w.mat_block_tables), t(w.seq_lens),
-                                 w.max_kv_len, w.mat_shared, out, indptr, w.mat_num_pages, "HND",
-                                 tbl, zero_tables, status, v_block_scales_layout="interleaved4")
-    torch.cuda.synchronize()
-    assert int(status.item()) & ~nv.DEV_LEN_CLAMPED == 0
-    got = out.view(torch.uint8).cpu().numpy()
-    bad = np.argwhere(got != want)
+    r = PL.run_materialize_interleaved(w, kc, vc, extra_out_pages, zero_tables, use_class)
+    assert r.status & ~nv.DEV_LEN_CLAMPED == 0
+    bad = np.argwhere(r.got != r.want)
     assert bad.size == 0, f"{len(bad)} FP8 bytes differ, first at {bad[0].tolist()}"
-    assert np.array_equal(tbl.cpu().numpy(), want_tbl)
-    return got
+    assert np.array_equal(r.got_tables, r.want_tables)
+    return r.got
 
 
 CASES = [
@@ -144,8 +98,8 @@ def test_interleaved_equals_linear_copy():
     kc, vc = _random_caches(w, 0, 0, 520)
     got = _compare(w, kc, vc)
     dev = torch.device("cuda")
-    kd, ks = _to_dev(w, kc, dev)
-    vd, vs = _to_dev(w, vc, dev)
+    kd, ks = PL.hnd_views(w, kc, dev)
+    vd, vs = PL.hnd_views(w, vc, dev)
     out = torch.full(got.shape, PL.SENT_FP8, dtype=torch.uint8,
                      device=dev).view(torch.float8_e4m3fn)
     nv.nvfp4_materialize_fp8(kd, vd, ks, vs, torch.as_tensor(w.mat_block_tables).to(dev),

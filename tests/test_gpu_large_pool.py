@@ -3,6 +3,10 @@ the launch configuration bench.py times (its Step: device-held global scales, ap
 dequant, materialize), checked against the CPU oracle: the two global scales over the whole
 tensors bit-exactly, and three sampled requests (the first, one drawn at random, the last)
 byte by byte -- their cache pages, their dequantized rows and their FP8 pages and table row.
+The sampled requests are rebuilt by the oracle from the workload's rows and the oracle's own
+global scales. The same run also materializes from V scales rewritten in the
+4-token-interleaved layout (the call bench.py makes with --v-scales interleaved4), checked on
+the same requests against the oracle's interleaved materialize.
 """
 import numpy as np
 import pytest
@@ -24,22 +28,34 @@ def ran(gpu_lib):
     w = W.large_pool(device="cuda")
     step = bench.Step(w, dev)
     step.run()
+    # the interleaved-V materialize of the same cache, into a second copy
+    P, H, ps, nb = step.sf[1].shape
+    v_il = step.sf[1].view(P, H, ps // 4, 4, nb).transpose(3, 4).contiguous().view(P, H, ps, nb)
+    fp8_il = torch.full_like(step.fp8.view(torch.uint8), 0x5A).view(torch.float8_e4m3fn)
+    tables_il = torch.full_like(step.tables, -7)
+    status_il = torch.zeros_like(step.status)
+    step.nv.nvfp4_materialize_fp8(
+        step.cache[0], step.cache[1], step.sf[0], v_il, step.mat_bt, step.seq_lens,
+        w.max_kv_len, w.mat_shared, fp8_il, step.indptr, w.mat_num_pages, step.lay, tables_il,
+        True, status_il, v_block_scales_layout="interleaved4")
     torch.cuda.synchronize()
-    return w, step
+    del v_il
+    r = PL.oracle_recipe(w.recipe)
+    gs = tuple(float(O.global_scale(W.bits16(x.cpu()), True, r)) for x in (w.k, w.v))
+    return w, step, gs, (fp8_il, tables_il, status_il)
 
 
 def test_global_scales_and_status(ran):
-    w, step = ran
+    w, step, gs, il = ran
     assert int(step.status.item()) == 0
-    r = PL.oracle_recipe(w.recipe)
-    for x, g in ((w.k, step.gk), (w.v, step.gv)):
-        want = O.global_scale(W.bits16(x.cpu()), True, r)
+    assert int(il[2].item()) == 0
+    for g, want in ((step.gk, gs[0]), (step.gv, gs[1])):
         assert np.float32(g.item()) == np.float32(want)
 
 
 @pytest.mark.parametrize("which", ["first", "random", "last"])
 def test_sampled_request(ran, which):
-    w, step = ran
+    w, step, (gs_k, gs_v), (fp8_il, tables_il, _) = ran
     b = {"first": 0, "random": int(np.random.default_rng(5).integers(1, w.B - 1)),
          "last": w.B - 1}[which]
     rows = np.flatnonzero(w.batch_indices == b)
@@ -48,7 +64,6 @@ def test_sampled_request(ran, which):
     ps, H, D = w.ps, w.H, w.D
     npg = -(-n // ps)
     r = PL.oracle_recipe(w.recipe)
-    gs_k, gs_v = float(step.gk.item()), float(step.gv.item())
     idx = torch.from_numpy(rows).to(w.k.device)
     kb, vb = W.bits16(w.k[idx].cpu()), W.bits16(w.v[idx].cpu())
     # the request alone, in a compact cache of its own pages (HND pages of [H, ps, .])
@@ -90,3 +105,16 @@ def test_sampled_request(ran, which):
         valid = min(ps, n - j * ps)
         assert np.array_equal(got[j][:, :, :valid], fp8[j + 1][:, :, :valid]), j
     assert not step.fp8.view(torch.uint8)[0].any()
+    # the same pages materialized from interleaved V scales
+    vil = O.PagedCache(vc.data, O.interleave4_scales(vc.sf.reshape(npg, H, ps, D // 16)).reshape(-1),
+                       dps, sps)
+    fp8i = np.zeros_like(fp8)
+    tabi = np.zeros_like(tab)
+    O.materialize_fp8(kc, vil, ps, H, D, w.layout, np.arange(npg, dtype=np.int32)[None], True,
+                      np.array([n], np.int32), n, None, fp8i, tabi, v_interleaved4=True)
+    assert np.array_equal(tables_il[b].cpu().numpy(), trow)
+    goti = fp8_il.view(torch.uint8)[torch.from_numpy(trow[:npg].astype(np.int64)).cuda()].cpu().numpy()
+    for j in range(npg):
+        valid = min(ps, n - j * ps)
+        assert np.array_equal(goti[j][:, :, :valid], fp8i[j + 1][:, :, :valid]), j
+    assert not fp8_il.view(torch.uint8)[0].any()
