@@ -287,6 +287,18 @@ class Step:
     def run(self, ev=None, flush=None):
         run_ops(self._ops, ev, flush)
 
+    def diagnostics(self):
+        """Share of the FP8 copy's active-page elements at +-448, the E4M3 maximum: the
+        products e2m1 * S that saturated, plus any exactly equal to 448. Read once, after
+        the timed steps."""
+        pages = self.tables[self.tables > 0].flatten()
+        fp8 = self.fp8.view(torch.uint8)
+        at_max = 0
+        for c in torch.split(pages.long(), 4096):
+            at_max += int(((fp8[c] & 0x7F) == 0x7E).sum().item())
+        total = pages.numel() * fp8[0].numel()
+        return {"materialize_fp8_at_448_fraction": at_max / total if total else 0.0}
+
     def op_bytes(self):
         return op_bytes(self.w, active_pages(self.w))
 
@@ -467,9 +479,16 @@ def cpu_baseline(w: W.Workload, target_s: float = 15.0):
         n = min(w.B, max(n + 1, int(n * min(8.0, target_s / 2 / max(dt, 1e-3)))))
         sub, nbytes = oracle_sample(w, n)
         dt = time_oracle(sub)
+    # the same oracle on one core, on a smaller sample (whole requests up to 4096 tokens)
+    one, one_bytes = oracle_sample(w, 0, max_tokens=4096)
+    dt1 = time_oracle(one, nthreads=1)
+    n1 = int(one.seq_lens.astype(np.int64).sum())
     return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"first {n} of {w.B} requests ({sub.nnz} tokens) of the {w.name} workload, "
-                      f"whole step, {dt:.1f} s"}
+                      f"whole step, {dt:.1f} s",
+            "single_thread": {"value": one_bytes / dt1 / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": f"first {n1} cached tokens ({one.B} requests), "
+                                        f"whole step, {dt1:.1f} s"}}
 
 
 def reference_arm(args, w: W.Workload):
@@ -625,6 +644,7 @@ def main():
     dom = max(step.NAMES[1:], key=lambda k: op_ms[k])
     value = world * total_bytes / (ms * 1e-3) / 1e9
     status = int(step.status.item())
+    diag = step.diagnostics() if isinstance(step, Step) else None
 
     e2e = None
     if not args.no_e2e:
@@ -653,6 +673,7 @@ def main():
                          "traffic": traffic_per_launch(dom, ntok[dom])},
             "clocks": clk, "gpu_launches": step.launches_per_step * args.steps,
             "e2e": e2e, "cpu_baseline": cpu, "device_status": status,
+            "diagnostics": diag,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
