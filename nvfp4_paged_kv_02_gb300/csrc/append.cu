@@ -25,8 +25,8 @@
 // binary16 sums run it as packed two-lane adds, pairs (2k, 2k+1)). B is kept only when its
 // error is strictly smaller.
 //
-// Per-CTA shared tables, indexed by scale byte: 1/(S*gs) (both tensors), (S, S) as half2,
-// and -sg as half2 (both tensors).
+// Per-CTA shared tables, indexed by scale byte: 1/(S*gs) (both tensors), and (S, S) as half2
+// (binary32 error) or -sg as half2 (binary16 error, both tensors).
 #include <cfloat>
 #include <type_traits>
 
@@ -210,10 +210,15 @@ __device__ __forceinline__ float candidate_f16(const float x[16], const uint32_t
   return __half2float(s);
 }
 
-struct Tables {
-  float inv[2][256];       // 1 / (S * gs) per tensor
-  uint32_t neg_sg2[2][256];  // (-RN16(S * RN16(gs))) in both halves, per tensor
-  uint32_t S2[256];        // (S, S) as half2
+// Per-CTA tables indexed by scale byte. The binary32-error recipes read both of a
+// candidate's constants with one 8-byte shared-memory load (measured faster there; the
+// other recipes measured faster with separate arrays).
+union Tables {
+  struct {
+    float inv[2][256];         // 1 / (S * gs) per tensor
+    uint32_t neg_sg2[2][256];  // (-RN16(S * RN16(gs))) in both halves, per tensor
+  } split;                     // standard NVFP4 and the binary16-error recipes
+  uint2 pair[2][256];          // binary32-error recipes: (bits of 1 / (S * gs), (S, S) as half2)
 };
 
 struct BlockOut {
@@ -234,7 +239,7 @@ __device__ __forceinline__ BlockOut quantize_block(const U32x8& in, const Tensor
   BlockOut r;
   if (MODE == 0) {
     r.s = e4m3x2_from_f32(ra, 0.0f) & 0xFFu;
-    const float inv = tab.inv[kv][r.s];
+    const float inv = tab.split.inv[kv][r.s];
     r.c0 = codes8(x, inv);
     r.c1 = codes8(x + 8, inv);
     return r;
@@ -248,15 +253,18 @@ __device__ __forceinline__ BlockOut quantize_block(const U32x8& in, const Tensor
   uint32_t a0, a1, b0, b1;
   float ea, eb;
   if (MODE == 1 || MODE == 2) {
-    ea = candidate_f32<MODE == 2>(x, tab.inv[kv][sa], tab.S2[sa], -tc.gs, a0, a1);
-    eb = candidate_f32<MODE == 2>(x, tab.inv[kv][sb], tab.S2[sb], -tc.gs, b0, b1);
+    const uint2 ta = tab.pair[kv][sa], tb = tab.pair[kv][sb];
+    ea = candidate_f32<MODE == 2>(x, __uint_as_float(ta.x), ta.y, -tc.gs, a0, a1);
+    eb = candidate_f32<MODE == 2>(x, __uint_as_float(tb.x), tb.y, -tc.gs, b0, b1);
   } else {
     uint32_t xh[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) xh[k] = BF16 ? f16x2_from_f32(x[2 * k], x[2 * k + 1]) : in.w[k];
     const uint32_t nzh2 = (nz >> 16) | nz;  // binary16 -0 in both halves
-    ea = candidate_f16<MODE == 4>(x, xh, tab.inv[kv][sa], tab.neg_sg2[kv][sa], nzh2, a0, a1);
-    eb = candidate_f16<MODE == 4>(x, xh, tab.inv[kv][sb], tab.neg_sg2[kv][sb], nzh2, b0, b1);
+    ea = candidate_f16<MODE == 4>(x, xh, tab.split.inv[kv][sa], tab.split.neg_sg2[kv][sa], nzh2,
+                                  a0, a1);
+    eb = candidate_f16<MODE == 4>(x, xh, tab.split.inv[kv][sb], tab.split.neg_sg2[kv][sb], nzh2,
+                                  b0, b1);
   }
   const bool take_b = eb < ea;
   r.c0 = take_b ? b0 : a0;
@@ -283,19 +291,25 @@ __device__ __forceinline__ bool load_scales(const AppendArgs& a, float gs[2]) {
 }
 
 // Fill the per-CTA tables for both tensors' global scales; ends with __syncthreads().
+template <int MODE>
 __device__ __forceinline__ void fill_tables(Tables& tab, const float gs[2]) {
   for (int s = threadIdx.x; s < 256; s += blockDim.x) {
     const uint32_t S2 = f16x2_from_e4m3x2(static_cast<uint32_t>(s) * 0x0101u);
     const float S = f32_from_f16_lo(S2);
-    tab.S2[s] = S2;
 #pragma unroll
     for (int kv = 0; kv < 2; ++kv) {
       const float den = __fmul_rn(S, gs[kv]);
-      tab.inv[kv][s] = den == 0.0f ? 0.0f : fminf(__frcp_rn(den), FLT_MAX);
-      const __half gh = __float2half_rn(gs[kv]);
-      const __half sg = __hmul_rn(__ushort_as_half(static_cast<unsigned short>(S2 & 0xFFFFu)), gh);
-      const uint32_t n = static_cast<uint32_t>(__half_as_ushort(sg)) ^ 0x8000u;
-      tab.neg_sg2[kv][s] = n | (n << 16);
+      const float inv = den == 0.0f ? 0.0f : fminf(__frcp_rn(den), FLT_MAX);
+      if (MODE == 1 || MODE == 2) {
+        tab.pair[kv][s] = make_uint2(__float_as_uint(inv), S2);
+      } else {
+        const __half gh = __float2half_rn(gs[kv]);
+        const __half sg =
+            __hmul_rn(__ushort_as_half(static_cast<unsigned short>(S2 & 0xFFFFu)), gh);
+        const uint32_t n = static_cast<uint32_t>(__half_as_ushort(sg)) ^ 0x8000u;
+        tab.split.inv[kv][s] = inv;
+        tab.split.neg_sg2[kv][s] = n | (n << 16);
+      }
     }
   }
   __syncthreads();
@@ -343,7 +357,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   __shared__ Tables tab;
   float gs[2];
   if (!load_scales(a, gs)) return;
-  fill_tables(tab, gs);
+  fill_tables<MODE>(tab, gs);
   const TensorConsts tck = make_consts(gs[0]);
   const TensorConsts tcv = make_consts(gs[1]);
 
@@ -506,7 +520,7 @@ __global__ void __launch_bounds__(append_threads(MODE), kAppendCtasPerSm)
     *s_abort = 0;
     fence_mbar_init();
   }
-  fill_tables(tab, gs);  // ends with __syncthreads()
+  fill_tables<MODE>(tab, gs);  // ends with __syncthreads()
 
   const int64_t tiles = (a.nnz + L.rows - 1) / L.rows;
   const uint32_t tile_bytes = L.rows * L.row_bytes;
