@@ -44,8 +44,11 @@ int current_device() {
 
 PipeTest pipe_test_from_env() {
   const char* v = std::getenv("NVFP4KV_TEST_STALL_PIPELINE");
-  if (v != nullptr && v[0] == '1') return PipeTest{1u << 12, 1};
-  return PipeTest{kWaitLimit, 0};
+  PipeTest t = (v != nullptr && v[0] == '1') ? PipeTest{1u << 12, 1, 0} : PipeTest{kWaitLimit, 0, 0};
+  const char* k = std::getenv("NVFP4KV_TEST_APPEND_KERNEL");
+  if (k != nullptr && std::strcmp(k, "ring") == 0) t.append_kernel = 1;
+  if (k != nullptr && std::strcmp(k, "direct") == 0) t.append_kernel = 2;
+  return t;
 }
 
 int sm_count() {

@@ -63,10 +63,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
 }
 
 // Test control of a pipelined launch: `stall` makes the producer withhold the first stage
-// of each CTA (so the consumers' wait expires), with a short `wait_limit`.
+// of each CTA (so the consumers' wait expires), with a short `wait_limit`. `append_kernel`
+// overrides the append's size-based kernel choice: 0 by size, 1 the TMA ring, 2 the
+// direct-load kernel (so that tests cover both at any size).
 struct PipeTest {
   uint32_t wait_limit;
   int32_t stall;
+  int32_t append_kernel;
 };
 
 // Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from global to

@@ -21,6 +21,23 @@ def has_gpu() -> bool:
         return False
 
 
+@pytest.fixture(params=["ring", "direct"])
+def append_kernel(request):
+    """Run a test once with each append kernel: the TMA ring and the direct-load kernel.
+    The library picks one by the size of the call; the host switch
+    NVFP4KV_TEST_APPEND_KERNEL (read on every call) overrides that choice, so both kernels
+    meet every case."""
+    old = os.environ.get("NVFP4KV_TEST_APPEND_KERNEL")
+    os.environ["NVFP4KV_TEST_APPEND_KERNEL"] = request.param
+    try:
+        yield request.param
+    finally:
+        if old is None:
+            os.environ.pop("NVFP4KV_TEST_APPEND_KERNEL", None)
+        else:
+            os.environ["NVFP4KV_TEST_APPEND_KERNEL"] = old
+
+
 @pytest.fixture(scope="session")
 def gpu_lib():
     """The CUDA library, built for sm_103a. On a GPU machine a missing or broken build is

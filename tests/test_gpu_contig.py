@@ -2,7 +2,8 @@
 nvfp4_kv_dequantize) through the C ABI against the CPU oracle, bit-exact on the packed
 codes, the scale bytes and the dequantized fp16/bf16 values. Sizes span several pipeline
 tiles with a ragged tail, strided input rows, rows too long for a shared-memory stage (the
-direct-load kernel), the recipes and both dtypes."""
+direct-load kernel), the recipes and both dtypes. Every test runs once with each quantize
+kernel (the TMA ring and the direct-load kernel)."""
 import numpy as np
 import pytest
 import torch
@@ -10,7 +11,7 @@ import torch
 import oracle as O
 import workloads as W
 
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("append_kernel")]
 
 
 @pytest.fixture(scope="module", autouse=True)

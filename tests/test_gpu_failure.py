@@ -29,10 +29,13 @@ def _cuda(gpu_lib):
 @pytest.fixture
 def stall_env():
     os.environ["NVFP4KV_TEST_STALL_PIPELINE"] = "1"
+    # a call this small would run the append's direct-load kernel, which has no ring
+    os.environ["NVFP4KV_TEST_APPEND_KERNEL"] = "ring"
     try:
         yield
     finally:
         os.environ.pop("NVFP4KV_TEST_STALL_PIPELINE", None)
+        os.environ.pop("NVFP4KV_TEST_APPEND_KERNEL", None)
 
 
 def _case():

@@ -4,6 +4,7 @@ Bit-exact on every byte the operations write (packed codes, scale bytes, dequant
 fp16/bf16, FP8 bytes, page tables) and on every byte they must leave alone (sentinels), for
 the named workloads at full size and a sweep of small ragged cases over layouts, dtypes,
 page sizes, head dims, table dtypes, recipes, tuple/stacked caches and padded page strides.
+Every test runs once with each append kernel (the TMA ring and the direct-load kernel).
 """
 import numpy as np
 import pytest
@@ -13,7 +14,7 @@ import oracle as O
 import workloads as W
 from tests import pipelines as PL
 
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("append_kernel")]
 
 
 @pytest.fixture(scope="module", autouse=True)
