@@ -238,7 +238,9 @@ class Step:
         self.gv = torch.empty(1, dtype=torch.float32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.lay = "NHD" if w.layout == W.NHD else "HND"
-        self.launches_per_step = 7  # 2 x (amax + finalize), append, dequant, materialize
+        # per tensor: one launch for a global scale of at most 2^16 elements, else amax + finalize
+        gs_launches = 1 if self.k.numel() <= (1 << 16) else 2
+        self.launches_per_step = 2 * gs_launches + 3  # 2 global scales, append, dequant, materialize
         if w.prefill_k is not None:
             # rows already in the cache before the measured append (untimed)
             pk, pv = w.prefill_k.to(dev), w.prefill_v.to(dev)
@@ -350,7 +352,8 @@ class ContigStep:
         self.gk = torch.empty(1, dtype=torch.float32, device=dev)
         self.gv = torch.empty(1, dtype=torch.float32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.launches_per_step = 8  # 2 x (amax + finalize), 2 quantize, 2 dequantize
+        gs_launches = 1 if self.k.numel() <= (1 << 16) else 2
+        self.launches_per_step = 2 * gs_launches + 4  # 2 global scales, 2 quantize, 2 dequantize
         self._ops = [self._global_scales, self._quantize, self._dequantize]
 
     def _global_scales(self):

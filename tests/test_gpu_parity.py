@@ -241,7 +241,8 @@ def test_device_bounds_flags():
     assert int(st.item()) == nv.DEV_BAD_OUT_PAGE
 
 
-@pytest.mark.parametrize("numel", [0, 1, 15, 16, 17, 1000, 4096 * 7 + 5, 3 << 20])
+@pytest.mark.parametrize("numel", [0, 1, 15, 16, 17, 1000, 4096 * 7 + 5, 1 << 16, (1 << 16) + 1,
+                                   (1 << 16) + 31, 3 << 20])
 @pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
 def test_global_scale(numel, dt):
     import nvfp4_paged_kv_02_gb300 as nv
@@ -251,6 +252,21 @@ def test_global_scale(numel, dt):
         got = nv.nvfp4_make_global_scale(x.cuda(), recipe).item()
         want = O.global_scale(W.bits16(x), dt == torch.bfloat16, orecipe)
         assert np.float32(got).view(np.uint32) == np.float32(want).view(np.uint32), (got, want)
+
+
+@pytest.mark.parametrize("numel", [1000, 1 << 16, (1 << 16) + 17, 1 << 20])
+@pytest.mark.parametrize("where", [0, -1, "mid"])
+def test_global_scale_max_at_edges(numel, where):
+    """The tensor's largest magnitude (negative) at the first, last or a middle element, for
+    sizes scanned by one CTA and by many."""
+    import nvfp4_paged_kv_02_gb300 as nv
+    x = (torch.randn(numel, generator=torch.Generator().manual_seed(numel)) * 0.5)
+    i = numel // 2 + 3 if where == "mid" else where
+    x[i] = -1000.0
+    x = x.to(torch.bfloat16)
+    got = nv.nvfp4_make_global_scale(x.cuda()).item()
+    want = O.global_scale(W.bits16(x), True, None)
+    assert np.float32(got).view(np.uint32) == np.float32(want).view(np.uint32), (got, want)
 
 
 def test_append_with_device_scales():
