@@ -173,7 +173,12 @@ nvfp4_status nvfp4_make_global_scale(const void* x, int32_t dtype, int64_t numel
  *                      pages say the space must already be described by these tables).
  *   k_scale, v_scale   global decode scales, positive finite.
  *   recipe             NULL = standard NVFP4; otherwise the 4over6 recipe.
- * Requirements: head_dim % 16 == 0, num_kv_heads >= 1, page_size >= 1, nnz >= 0. */
+ * Requirements: head_dim % 16 == 0, num_kv_heads >= 1, page_size >= 1, nnz >= 0.
+ * Kernels: a call of at most 2^18 blocks per tensor (nnz * H * D / 16; a decode step of up
+ * to 4096 tokens at 8 heads of 128) runs a direct-load kernel, which starts sooner; larger
+ * calls run a shared-memory ring fed by bulk copies. Both write the same bytes. The
+ * environment variable NVFP4KV_TEST_APPEND_KERNEL=ring|direct, read on every call, overrides
+ * the choice (for tests). nvfp4_kv_quantize makes the same choice. */
 nvfp4_status nvfp4_quantize_append_paged(
     const void* append_key, const void* append_value, int32_t dtype, int64_t nnz,
     int32_t num_kv_heads, int32_t head_dim, int64_t key_row_stride, int64_t value_row_stride,
