@@ -48,9 +48,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
     """Compile (if stale) and return the path of libnvfp4kv.so."""
     stamp = _stamp()
     stamp_file = os.path.join(BUILD_DIR, "stamp")
-    if (not force and os.path.exists(LIB_PATH) and os.path.exists(stamp_file)
-            and open(stamp_file).read() == stamp):
-        return LIB_PATH
+    if not force and os.path.exists(LIB_PATH) and os.path.exists(stamp_file):
+        with open(stamp_file) as f:
+            if f.read() == stamp:
+                return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
     exe = nvcc()
 

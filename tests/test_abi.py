@@ -16,7 +16,8 @@ HEADER = os.path.join(ROOT, "include", "nvfp4kv.h")
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\**\s+\**(nvfp4_\w+)\s*\(", text, re.M)))
 

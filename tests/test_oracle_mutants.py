@@ -97,7 +97,8 @@ MUTANTS = {
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_mutant_is_caught(name, tmp_path):
     old, new = MUTANTS[name]
-    src = open(SRC).read()
+    with open(SRC) as f:
+        src = f.read()
     assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
     path = tmp_path / "mutant.c"
     path.write_text(src.replace(old, new))
