@@ -146,7 +146,8 @@ float nvfp4_e4m3_max(const nvfp4_4over6_config* recipe);
  *   numel      >= 0.
  *   scale_out  device, one float, overwritten (it is also the reduction's accumulator, so
  *              it must not alias x).
- * Enqueues a 4-byte memset and two kernels. */
+ * A tensor of at most 65,536 elements is one kernel launch (one CTA scans it and writes gs);
+ * a larger one enqueues a 4-byte memset and two kernels (a many-CTA scan, then gs). */
 nvfp4_status nvfp4_make_global_scale(const void* x, int32_t dtype, int64_t numel,
                                      const nvfp4_4over6_config* recipe, float* scale_out,
                                      void* stream);
