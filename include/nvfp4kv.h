@@ -55,7 +55,7 @@ extern "C" {
 typedef int32_t nvfp4_status;
 #define NVFP4_OK 0
 #define NVFP4_ERR_INVALID_ARG 1 /* a size, enum, scale or extent is out of range */
-#define NVFP4_ERR_UNSUPPORTED 2 /* a valid request this build does not implement */
+#define NVFP4_ERR_UNSUPPORTED 2 /* a valid request this library does not implement */
 #define NVFP4_ERR_ALIGNMENT 3   /* a pointer or stride breaks the stated alignment */
 #define NVFP4_ERR_CUDA 4        /* the CUDA runtime reported an error at launch */
 
