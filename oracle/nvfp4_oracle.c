@@ -33,10 +33,14 @@
  * casts and brute force; the block quantization against exact rational arithmetic; the
  * paged addressing against numpy views of the documented tensor shapes; dequant and the
  * FP8 copy against numpy binary32 arithmetic over every (code, scale) pair.
- * Parity unpinned, in part: two readings have no outside reference -- the order of the
- * 4over6 error sum and the reciprocal form of the element scaling x * (1/(S*gs)). The pins
- * fix every result whose rounding decisions are clear of a midpoint and whose candidate
- * errors are not near-tied; the outcomes inside those bands follow the readings alone.
+ * Parity unpinned, in part: four readings have no outside reference -- the reciprocal form
+ * of the element scaling x * (1/(S*gs)), the order of the 4over6 error sum, and the
+ * rounding steps of the 4over6 element error in binary32 (one fused rounding) and in
+ * binary16 (operands rounded to binary16, then one fused rounding). The pins fix every
+ * result whose rounding decisions are clear of a midpoint and whose candidate errors are
+ * not near-tied; the outcomes inside those bands follow the readings alone. An independent
+ * restatement of the readings (tests/pins.py, exact rational arithmetic) checks that this
+ * file computes them as stated.
  * Parity unpinned: the 4-token-interleaved V-scale layout of the materialize input. The
  * pages name it without defining it; the reading (interleaved4_sf_offset) is pinned only
  * against a second expression of itself, the layout writer in oracle/__init__.py.
@@ -235,13 +239,20 @@ static double tree16_f16(double t[16]) {
 }
 
 /* Reconstruction error of a candidate ([P4]: each candidate is quantized and then
- * dequantized, and the reconstructions are compared). Reading: the element error is
- * x - e2m1(q)*S*gs computed exactly and rounded once (a fused multiply-add), as the page
- * calls the fp32 evaluation exact; the summed term is |e| (MAE) or e*e rounded (MSE).
- * With fast math ([P4] err_use_fast_math, a half-precision evaluation) every step is a
- * binary16 operation: x and gs are rounded to binary16, the block's decode factor is
- * sg = RN16(S * gs_h), the element error is e = RN16(x_h - e2m1(q) * sg) (fused), and e*e
- * and each partial sum are rounded to binary16. */
+ * dequantized, and the reconstructions are compared). One rule in both precisions: the
+ * element error is the residual x - e2m1(q)*S*gs, formed from operands of the evaluation's
+ * precision and rounded once to that precision (a fused multiply-add), the product taken in
+ * the order the decode rule is written, (e2m1 value * block scale) * global scale ([P2] k_scale
+ * / v_scale parameter: e2m1_value * block_scale * global_scale).
+ *   binary32 (the default, which [P4] calls exact): e = RN32(x - (e2m1(q)*S)*gs); e2m1*S is
+ *     exact in binary32, so the one rounding is that of the residual.
+ *   binary16 ([P4] err_use_fast_math, the error evaluated in fp16): the operands become
+ *     binary16 first, x_h = RN16(x) and g_h = RN16(gs) (e2m1*S is exact in binary16), and
+ *     e = RN16(x_h - (e2m1(q)*S)*g_h).
+ * The summed term is |e| (MAE) or e*e rounded to the precision (MSE); the partial sums are
+ * rounded to it as well. Parity unpinned: the pages fix neither the rounding steps nor the
+ * association; tests/pins.py restates this reading independently, which pins this code to
+ * the reading, not the reading to the pages. */
 static double block_error(const float x[16], const uint32_t q[16], uint32_t s, float gs,
                           const oracle_recipe* r) {
   double S = oracle_e4m3_decode(s);
@@ -257,11 +268,10 @@ static double block_error(const float x[16], const uint32_t q[16], uint32_t s, f
   }
   double t[16];
   double gh = f16_round((double)gs);
-  double sg = f16_round(S * gh); /* S*gh is exact in double */
   for (int i = 0; i < 16; ++i) {
     double xh = f16_round((double)x[i]);
-    double v = oracle_e2m1_decode(q[i]);
-    double e = f16_round(fma(-v, sg, xh)); /* exact in double before the one rounding */
+    double w = oracle_e2m1_decode(q[i]) * S; /* exact: at most 6 significant bits */
+    double e = f16_round(fma(-w, gh, xh));   /* w*gh is exact in double; one rounding */
     t[i] = mse ? f16_round(e * e) : fabs(e);
   }
   return tree16_f16(t);

@@ -42,6 +42,16 @@ MUTANTS = {
     "mae_signed_error": ("t[i] = mse ? e * e : fabsf(e);", "t[i] = mse ? e * e : e;"),
     "error_sign_flipped": ("float e = fmaf(-w, gs, x[i]);", "float e = fmaf(w, gs, x[i]);"),
     "fast_math_ignored": ("if (!r->err_use_fast_math) {", "if (1) {"),
+    # other plausible rounding steps of the 4over6 element error (readings R6, R7)
+    "error_f32_unfused": ("float e = fmaf(-w, gs, x[i]);", "float e = x[i] - w * gs;"),
+    "fast_math_decode_factor_rounded": (
+        "double e = f16_round(fma(-w, gh, xh));",
+        "double e = f16_round(fma(-oracle_e2m1_decode(q[i]), f16_round(S * gh), xh));"),
+    "fast_math_dequant_in_f32": (
+        "double e = f16_round(fma(-w, gh, xh));",
+        "double e = f16_round(xh - f16_round((double)((float)w * gs)));"),
+    "fast_math_unfused": (
+        "double e = f16_round(fma(-w, gh, xh));", "double e = f16_round(xh - f16_round(w * gh));"),
     "fast_math_keeps_gs_exact": ("double gh = f16_round((double)gs);",
                                  "double gh = (double)gs * 3.0;"),
     "global_scale_ignores_recipe": (
