@@ -241,7 +241,8 @@ nvfp4_status nvfp4_materialize_fp8_out_pages(int32_t batch_size, int32_t max_kv_
  *   NULL),
  * out[o, 0|1, h, slot, d] = E4M3_RNE_satfinite(e2m1(q) * S) for every slot of the page
  * (K at 0, V at 1; no global scale), page 0 is set to zero, fp8_block_tables[b, j] = o.
- * Pages past each request's length and past kv_page_indptr[batch_size] are not written.
+ * Nothing is written for columns j >= ceil(seq_lens[b] / page_size) of request b, nor to
+ * output pages above kv_page_indptr[batch_size] ("nvfp4_kv_materialize_fp8": returns).
  *   block_tables   device int32 [batch_size, max_num_pages] when uses_shared_paged_kv_idx,
  *                  else [batch_size, 2, max_num_pages] (K row then V row);
  *                  max_num_pages >= max_pages_per_seq.
