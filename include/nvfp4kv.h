@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define NVFP4KV_ABI_VERSION 2
+#define NVFP4KV_ABI_VERSION 3
 
 /* Return codes. */
 typedef int32_t nvfp4_status;
@@ -252,7 +252,7 @@ nvfp4_status nvfp4_materialize_fp8_out_pages(int32_t batch_size, int32_t max_kv_
  *   num_pages      host copy of kv_page_indptr[batch_size] (required with kv_page_indptr,
  *                  ignored without it).
  *   out            device float8_e4m3fn bytes, contiguous [out_num_pages, 2, H, page_size,
- *                  D], out_num_pages >= num_pages + 1, 16-byte aligned.
+ *                  D], out_num_pages >= num_pages + 1, 32-byte aligned.
  *   fp8_block_tables  device int32 [batch_size, max_pages_per_seq], contiguous.
  *   zero_fp8_block_tables  1: entries past each request's pages are set to 0 (the
  *                  functional API's padding); 0: they are left alone (run(), where the
@@ -268,6 +268,58 @@ nvfp4_status nvfp4_materialize_fp8(
     int32_t batch_size, int32_t max_kv_len, const int32_t* kv_page_indptr, int64_t num_pages,
     uint8_t* out, int64_t out_num_pages, int32_t* fp8_block_tables,
     int32_t zero_fp8_block_tables, int32_t v_scale_layout, int32_t* dev_status, void* stream);
+
+/* A materialize launch prepared once ("flashinfer.quantization" index, NVFP4KVMaterializer:
+ * the static layout is checked when the materializer is built, so that each run() costs
+ * the host little more than the launch). Caller-owned plain data: filled by
+ * nvfp4_materializer_prepare and only read afterwards. It holds no device memory and needs
+ * no release; copies are valid. */
+typedef struct {
+  int32_t page_size, num_kv_heads, head_dim, kv_layout;
+  int32_t uses_shared_paged_kv_idx, v_scale_layout;
+  int32_t max_batch_size;  /* the largest batch_size a run may pass */
+  int32_t device;          /* CUDA device current at prepare; runs must use it */
+  int64_t data_page_stride, sf_page_stride;  /* bytes between pages of both caches */
+  int32_t bulk, grid, smem_bytes;            /* launch shape chosen at prepare */
+  int32_t stall_test;                        /* NVFP4KV_TEST_STALL_PIPELINE at prepare */
+  uint32_t magic;                            /* set by a successful prepare */
+  int32_t reserved[3];
+} nvfp4_materializer;
+
+/* Check the static layout of a materialize loop once and choose its launch shape.
+ *   m                 caller-owned, written here (and on no other call).
+ *   page_size, num_kv_heads, head_dim, kv_layout, uses_shared_paged_kv_idx, v_scale_layout
+ *                     as for nvfp4_materialize_fp8, with the same requirements.
+ *   data_page_stride, sf_page_stride  page strides (bytes) that every run's K and V caches
+ *                     will have; at least one page each, data strides a multiple of 16,
+ *                     scale strides even.
+ *   max_batch_size    1..16384; each run's batch_size must not exceed it (the launch
+ *                     reserves shared memory for this many request lengths).
+ * Runs on the current device and opts the kernel in to its shared memory (no device
+ * memory is allocated and nothing is launched). Errors return the usual status codes and
+ * leave m unusable. The pipeline test switch NVFP4KV_TEST_STALL_PIPELINE is read here. */
+nvfp4_status nvfp4_materializer_prepare(nvfp4_materializer* m, int32_t page_size,
+                                        int32_t num_kv_heads, int32_t head_dim,
+                                        int32_t kv_layout, int32_t uses_shared_paged_kv_idx,
+                                        int32_t v_scale_layout, int64_t data_page_stride,
+                                        int64_t sf_page_stride, int32_t max_batch_size);
+
+/* One materialize with a prepared layout (NVFP4KVMaterializer.run): the arguments and
+ * results of nvfp4_materialize_fp8 with zero_fp8_block_tables = 0 (only the active
+ * entries of fp8_block_tables are written; the caller zeroes the table once per step),
+ * and max_kv_len given as max_pages_per_seq (the table's columns). Per call it checks only
+ * what can change between calls: that m was prepared on the current device, the caches'
+ * strides and base alignment, batch_size <= m->max_batch_size, the table widths, the
+ * output extent and null pointers. One kernel launch on `stream` (batch_size 0: a memset
+ * of the zero page); nothing allocated, no host synchronization. */
+nvfp4_status nvfp4_materializer_run(const nvfp4_materializer* m, nvfp4_paged_cache k_cache,
+                                    nvfp4_paged_cache v_cache, const int32_t* block_tables,
+                                    int32_t max_num_pages, const int32_t* seq_lens,
+                                    int32_t batch_size, int32_t max_pages_per_seq,
+                                    const int32_t* kv_page_indptr, int64_t num_pages,
+                                    uint8_t* out, int64_t out_num_pages,
+                                    int32_t* fp8_block_tables, int32_t* dev_status,
+                                    void* stream);
 
 /* Quantize a contiguous fp16/bf16 tensor to NVFP4 with linear block scales
  * ("flashinfer.quantization" index, "FP4 KV Cache Quantization": nvfp4_kv_quantize).

@@ -57,6 +57,18 @@ class _Cache(ctypes.Structure):
                 ("num_pages", ctypes.c_int64)]
 
 
+class _Materializer(ctypes.Structure):
+    """nvfp4_materializer: a materialize launch prepared once (plain data)."""
+    _fields_ = [("page_size", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("kv_layout", ctypes.c_int32),
+                ("uses_shared_paged_kv_idx", ctypes.c_int32), ("v_scale_layout", ctypes.c_int32),
+                ("max_batch_size", ctypes.c_int32), ("device", ctypes.c_int32),
+                ("data_page_stride", ctypes.c_int64), ("sf_page_stride", ctypes.c_int64),
+                ("bulk", ctypes.c_int32), ("grid", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
+                ("stall_test", ctypes.c_int32), ("magic", ctypes.c_uint32),
+                ("reserved", ctypes.c_int32 * 3)]
+
+
 class _Config(ctypes.Structure):
     _fields_ = [("e4m3_max", ctypes.c_float), ("err_mode", ctypes.c_int32),
                 ("err_use_fast_math", ctypes.c_int32)]
@@ -112,6 +124,11 @@ def load() -> ctypes.CDLL:
         L.nvfp4_materialize_fp8.argtypes = [
             _Cache, _Cache, i32, i32, i32, i32, vp, i32, i32, vp, i32, i32, vp, i64, vp, i64, vp,
             i32, i32, vp, vp]
+        L.nvfp4_materializer_prepare.restype = i32
+        L.nvfp4_materializer_prepare.argtypes = [vp, i32, i32, i32, i32, i32, i32, i64, i64, i32]
+        L.nvfp4_materializer_run.restype = i32
+        L.nvfp4_materializer_run.argtypes = [
+            vp, _Cache, _Cache, vp, i32, vp, i32, i32, vp, i64, vp, i64, vp, vp, vp]
         L.nvfp4_4over6_code.restype = i32
         L.nvfp4_4over6_code.argtypes = [vp, vp]
         L.nvfp4_4over6_from_code.restype = i32
@@ -369,15 +386,19 @@ def nvfp4_materialize_fp8(k_cache: torch.Tensor, v_cache: torch.Tensor,
 
 class NVFP4KVMaterializer:
     """Validate once, launch many times ("NVFP4KVMaterializer"): the static layout and the
-    device are checked at construction; run() launches on the current stream with
-    caller-owned outputs, allocates nothing and does not synchronize, so it can be captured
-    in a CUDA graph. It writes only the active table entries (the caller zeroes the table
-    once per step)."""
+    device are checked at construction (nvfp4_materializer_prepare); run() launches on the
+    current stream through nvfp4_materializer_run with caller-owned outputs, allocates
+    nothing and does not synchronize, so it can be captured in a CUDA graph. It writes only
+    the active table entries (the caller zeroes the table once per step).
+
+    The prepared launch is specific to the caches' page strides and reserves room for
+    `max_batch_size` requests; a run with other strides or a larger batch prepares again
+    (host work only, once per new shape)."""
 
     def __init__(self, num_kv_heads: int, page_size: int, head_dim: int,
                  device: Union[str, int, torch.device] = "cuda",
                  uses_shared_paged_kv_idx: bool = True, kv_layout: str = "HND",
-                 v_block_scales_layout: str = "linear"):
+                 v_block_scales_layout: str = "linear", max_batch_size: int = 256):
         if page_size % 4 != 0:
             raise ValueError("page_size must be divisible by 4")
         if head_dim % 64 != 0:
@@ -391,7 +412,26 @@ class NVFP4KVMaterializer:
         self.v_sf_layout = _sf_layout(v_block_scales_layout)
         if self.v_sf_layout == SF_INTERLEAVED4 and self.layout != HND:
             raise ValueError("4-token-interleaved V scales need HND pages")
+        if self.device.index is None:
+            self.device = torch.device("cuda", torch.cuda.current_device())
         self._lib = load()
+        self._prepared = {}
+        # the compact page layout, checked now so that a bad layout fails at construction
+        self._max_batch = int(max_batch_size)
+        self._prepare(self.ps * self.H * self.D // 2, self.ps * self.H * self.D // 16,
+                      self._max_batch)
+
+    def _prepare(self, dps: int, sps: int, max_batch: int) -> _Materializer:
+        key = (dps, sps, max_batch)
+        m = self._prepared.get(key)
+        if m is None:
+            m = _Materializer()
+            with torch.cuda.device(self.device):
+                _check("nvfp4_materializer_prepare", self._lib.nvfp4_materializer_prepare(
+                    ctypes.byref(m), self.ps, self.H, self.D, self.layout, int(self.shared),
+                    self.v_sf_layout, dps, sps, max_batch))
+            self._prepared[key] = m
+        return m
 
     def run(self, k_cache, v_cache, k_block_scales, v_block_scales, block_tables, seq_lens,
             kv_page_indptr, *, out: torch.Tensor, fp8_block_tables: torch.Tensor,
@@ -399,12 +439,13 @@ class NVFP4KVMaterializer:
         B, mpps = fp8_block_tables.shape
         kc = _one_cache(k_cache, k_block_scales)
         vc = _one_cache(v_cache, v_block_scales)
-        _check("nvfp4_materialize_fp8", self._lib.nvfp4_materialize_fp8(
-            kc._c(), vc._c(), self.ps, self.H, self.D, self.layout, _ptr(block_tables),
-            block_tables.shape[-1], int(self.shared), _ptr(seq_lens), B, mpps * self.ps,
-            _ptr(kv_page_indptr), out.shape[0] - 1, _ptr(out), out.shape[0],
-            _ptr(fp8_block_tables), 0, self.v_sf_layout, _ptr(dev_status),
-            _stream(self.device)))
+        if B > self._max_batch:
+            self._max_batch = 1 << (B - 1).bit_length()
+        m = self._prepare(kc.data_page_stride, kc.sf_page_stride, self._max_batch)
+        _check("nvfp4_materializer_run", self._lib.nvfp4_materializer_run(
+            ctypes.byref(m), kc._c(), vc._c(), _ptr(block_tables), block_tables.shape[-1],
+            _ptr(seq_lens), B, mpps, _ptr(kv_page_indptr), out.shape[0] - 1, _ptr(out),
+            out.shape[0], _ptr(fp8_block_tables), _ptr(dev_status), _stream(self.device)))
         return out, fp8_block_tables
 
 

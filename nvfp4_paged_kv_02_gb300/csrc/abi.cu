@@ -30,6 +30,15 @@ nvfp4_status check_launch(const char* what) {
   return NVFP4_OK;
 }
 
+nvfp4_status set_dynamic_smem(const void* kernel, size_t bytes, const char* what) {
+  const cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess) return NVFP4_OK;
+  (void)cudaGetLastError();  // the refusal must not surface as a later launch's error
+  return fail(NVFP4_ERR_CUDA, std::string(what) + ": cannot opt in to " + std::to_string(bytes) +
+                                  " bytes of dynamic shared memory: " + cudaGetErrorString(e));
+}
+
 namespace {
 std::mutex g_mu;
 std::unordered_map<int, int> g_sms;
@@ -532,6 +541,132 @@ NVFP4_EXPORT nvfp4_status nvfp4_materialize_fp8(
     return NVFP4_OK;
   }
   return launch_materialize(a, static_cast<cudaStream_t>(stream));
+}
+
+constexpr uint32_t kMaterializerMagic = 0x4E564D31u;  // "NVM1"
+
+NVFP4_EXPORT nvfp4_status nvfp4_materializer_prepare(
+    nvfp4_materializer* m, int32_t page_size, int32_t num_kv_heads, int32_t head_dim,
+    int32_t kv_layout, int32_t uses_shared_paged_kv_idx, int32_t v_scale_layout,
+    int64_t data_page_stride, int64_t sf_page_stride, int32_t max_batch_size) {
+  clear_error();
+  const char* fn = "nvfp4_materializer_prepare";
+  if (!m) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materializer_prepare: m is null");
+  m->magic = 0;
+  if (v_scale_layout != NVFP4_SF_LINEAR && v_scale_layout != NVFP4_SF_INTERLEAVED4)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materializer_prepare: v_scale_layout must be NVFP4_SF_LINEAR or NVFP4_SF_INTERLEAVED4");
+  if (nvfp4_status st = check_geometry(fn, page_size, num_kv_heads, head_dim, kv_layout)) return st;
+  if (head_dim % 64 != 0) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materializer_prepare: head_dim must be divisible by 64");
+  if (page_size % 4 != 0) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materializer_prepare: page_size must be divisible by 4");
+  if (v_scale_layout == NVFP4_SF_INTERLEAVED4 && kv_layout != NVFP4_HND)
+    return fail(NVFP4_ERR_UNSUPPORTED, "nvfp4_materializer_prepare: 4-token-interleaved V scales are defined for HND pages only");
+  if (max_batch_size < 1 || max_batch_size > kMaxScanBatch)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materializer_prepare: max_batch_size must be in [1, 16384]");
+  const int64_t cb = static_cast<int64_t>(page_size) * num_kv_heads * (head_dim / 2);
+  const int64_t sb = static_cast<int64_t>(page_size) * num_kv_heads * (head_dim / 16);
+  if (data_page_stride < cb || sf_page_stride < sb)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materializer_prepare: a page stride is smaller than a page");
+  if (data_page_stride % 16 != 0 || sf_page_stride % 2 != 0)
+    return fail(NVFP4_ERR_ALIGNMENT, "nvfp4_materializer_prepare: data page stride must be a multiple of 16 and scale page stride even");
+  // bulk copies also need 16-byte scale strides and a page that fits a stage (bases are
+  // checked per run)
+  const bool bulk = cb % 16 == 0 && sb % 16 == 0 && cb + sb <= 48 * 1024 && sf_page_stride % 16 == 0;
+  MaterializeLaunch c{};
+  if (nvfp4_status st = prepare_materialize(bulk, v_scale_layout == NVFP4_SF_INTERLEAVED4,
+                                            max_batch_size, cb, sb, &c))
+    return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(NVFP4_ERR_CUDA, "nvfp4_materializer_prepare: no current CUDA device");
+  }
+  const char* stall = std::getenv("NVFP4KV_TEST_STALL_PIPELINE");
+  *m = nvfp4_materializer{};
+  m->page_size = page_size;
+  m->num_kv_heads = num_kv_heads;
+  m->head_dim = head_dim;
+  m->kv_layout = kv_layout;
+  m->uses_shared_paged_kv_idx = uses_shared_paged_kv_idx ? 1 : 0;
+  m->v_scale_layout = v_scale_layout;
+  m->max_batch_size = max_batch_size;
+  m->device = dev;
+  m->data_page_stride = data_page_stride;
+  m->sf_page_stride = sf_page_stride;
+  m->bulk = c.bulk;
+  m->grid = c.grid;
+  m->smem_bytes = c.smem;
+  m->stall_test = (stall != nullptr && stall[0] == '1') ? 1 : 0;
+  m->magic = kMaterializerMagic;
+  return NVFP4_OK;
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_materializer_run(
+    const nvfp4_materializer* m, nvfp4_paged_cache k_cache, nvfp4_paged_cache v_cache,
+    const int32_t* block_tables, int32_t max_num_pages, const int32_t* seq_lens,
+    int32_t batch_size, int32_t max_pages_per_seq, const int32_t* kv_page_indptr,
+    int64_t num_pages, uint8_t* out, int64_t out_num_pages, int32_t* fp8_block_tables,
+    int32_t* dev_status, void* stream) {
+  clear_error();
+  if (!m || m->magic != kMaterializerMagic)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materializer_run: m was not prepared");
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != m->device)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materializer_run: the current device is not the one m was prepared on");
+  if (batch_size < 0 || batch_size > m->max_batch_size)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materializer_run: batch_size must be in [0, max_batch_size]");
+  if (max_pages_per_seq < 0 || max_num_pages < max_pages_per_seq)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materializer_run: block_tables needs at least max_pages_per_seq columns");
+  const nvfp4_paged_cache* cs[2] = {&k_cache, &v_cache};
+  for (const nvfp4_paged_cache* c : cs) {
+    if (c->data_page_stride != m->data_page_stride || c->sf_page_stride != m->sf_page_stride)
+      return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materializer_run: cache page strides differ from the prepared ones");
+    if (c->num_pages < 0 || (c->num_pages > 0 && (!c->data || !c->sf)))
+      return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materializer_run: bad cache pointers or num_pages");
+    if (!aligned(c->data, 16) || !aligned(c->sf, m->bulk ? 16 : 2))
+      return fail(NVFP4_ERR_ALIGNMENT, "nvfp4_materializer_run: cache data must be 16-byte aligned (scales too for this page shape)");
+  }
+  int64_t n = static_cast<int64_t>(batch_size) * max_pages_per_seq;
+  if (kv_page_indptr) {
+    if (num_pages < 0) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materializer_run: kv_page_indptr requires num_pages");
+    n = num_pages;
+  }
+  if (!out || !aligned(out, 32) || out_num_pages < n + 1 || n + 1 > (int64_t(1) << 31))
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materializer_run: out must be 32-byte aligned with num_pages + 1 (< 2^31) pages");
+  if (batch_size > 0 && (!block_tables || !seq_lens || !fp8_block_tables))
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materializer_run: null device pointer");
+  const int32_t ps = m->page_size, H = m->num_kv_heads, D = m->head_dim;
+  if (batch_size == 0) {
+    const size_t bytes = static_cast<size_t>(2) * H * ps * D;
+    const cudaError_t e = cudaMemsetAsync(out, 0, bytes, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, std::string("cudaMemsetAsync: ") + cudaGetErrorString(e));
+    return NVFP4_OK;
+  }
+  MaterializeArgs a{};
+  a.kc = k_cache;
+  a.vc = v_cache;
+  a.ps = ps;
+  a.H = H;
+  a.D = D;
+  a.layout = m->kv_layout;
+  a.div_page_chunks = make_div(static_cast<int64_t>(ps) * (D / 32));
+  a.div_row_chunks = make_div(D / 32);
+  a.div_mpps = make_div(max_pages_per_seq > 0 ? max_pages_per_seq : 1);
+  a.block_tables = block_tables;
+  a.max_num_pages = max_num_pages;
+  a.shared = m->uses_shared_paged_kv_idx;
+  a.seq_lens = seq_lens;
+  a.B = batch_size;
+  a.mpps = max_pages_per_seq;
+  a.kv_page_indptr = kv_page_indptr;
+  a.out = out;
+  a.out_num_pages = out_num_pages;
+  a.tables = fp8_block_tables;
+  a.zero_tables = 0;
+  a.v_interleaved = m->v_scale_layout == NVFP4_SF_INTERLEAVED4 ? 1 : 0;
+  a.pipe = m->stall_test ? PipeTest{1u << 12, 1, 0} : PipeTest{kWaitLimit, 0, 0};
+  a.status = dev_status;
+  const MaterializeLaunch c{m->bulk, m->max_batch_size, m->smem_bytes, m->grid};
+  return launch_materialize_prepared(a, c, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

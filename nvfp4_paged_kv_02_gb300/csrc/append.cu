@@ -17,16 +17,17 @@
 // rounded one, from a precomputed reciprocal of 6 gs (see div_rn_with_rcp).
 // 4over6: s_B = E4M3(min(amax / (4 gs), 448)) as well; each candidate's error sums, over the
 // block, |e_i| (MAE) or e_i^2 (MSE):
-//   binary32 error: e_i = x_i - e2m1(q_i) * S * gs, rounded once (e2m1 * S is exact in
-//                   binary16, the rest is one fused multiply-add);
-//   binary16 error: e_i = RN16(x_h - e2m1(q_i) * sg) with x_h = RN16(x_i) and
-//                   sg = RN16(S * RN16(gs)); squares and sums rounded to binary16.
+//   binary32 error: e_i = RN32(x_i - (e2m1(q_i) * S) * gs) (e2m1 * S is exact in binary16,
+//                   the rest is one fused multiply-add);
+//   binary16 error: the same residual from binary16 operands, rounded once to binary16:
+//                   e_i = RN16(x_h - (e2m1(q_i) * S) * g_h), x_h = RN16(x_i), g_h = RN16(gs);
+//                   squares and sums rounded to binary16.
 // The sum runs over a fixed halving tree: t[i] += t[i+8], t[i+4], t[i+2], t[i+1] (the
 // binary16 sums run it as packed two-lane adds, pairs (2k, 2k+1)). B is kept only when its
 // error is strictly smaller.
 //
 // Per-CTA shared tables, indexed by scale byte: 1/(S*gs) (both tensors), and (S, S) as half2
-// (binary32 error) or -sg as half2 (binary16 error, both tensors).
+// (the 4over6 recipes).
 #include <cfloat>
 #include <type_traits>
 
@@ -41,6 +42,7 @@ constexpr int kThreads = 256;
 // Per-tensor constants for one block quantization.
 struct TensorConsts {
   float gs;       // global decode scale
+  uint32_t neg_gh2;  // -RN16(gs) in both binary16 halves (binary16 error)
   float g6, r6;   // fp32(6 gs) and its reciprocal
   float g4, r4;   // 4 gs and its reciprocal
   bool exact_rcp; // both divisors and reciprocals are normal: use div_rn_with_rcp
@@ -49,6 +51,8 @@ struct TensorConsts {
 __device__ __forceinline__ TensorConsts make_consts(float gs) {
   TensorConsts c;
   c.gs = gs;
+  const uint32_t gh = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(gs))) ^ 0x8000u;
+  c.neg_gh2 = gh | (gh << 16);
   c.g6 = __fmul_rn(6.0f, gs);
   c.g4 = __fmul_rn(4.0f, gs);
   c.r6 = __frcp_rn(c.g6);
@@ -184,16 +188,18 @@ __device__ __forceinline__ float candidate_f32(const float x[16], float inv, uin
 }
 
 // One candidate with the binary16 error: codes c0, c1 and the error sum (as a float).
+// S2 = (S, S) and neg_gh2 = (-g_h, -g_h) as half2.
 template <bool MSE>
 __device__ __forceinline__ float candidate_f16(const float x[16], const uint32_t xh[8], float inv,
-                                               uint32_t neg_sg2, uint32_t nzh2, uint32_t& c0,
-                                               uint32_t& c1) {
+                                               uint32_t S2, uint32_t neg_gh2, uint32_t nzh2,
+                                               uint32_t& c0, uint32_t& c1) {
   uint32_t t[8];
   c0 = encode8(x, inv, t);
   c1 = encode8(x + 8, inv, t + 4);
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    const uint32_t e = hfma2_rn(t[k], neg_sg2, xh[k]);
+    const uint32_t w = hmul2_rn(t[k], S2);  // e2m1 * S, exact
+    const uint32_t e = hfma2_rn(w, neg_gh2, xh[k]);  // x_h - w * g_h, one rounding
     if (MSE) {
       t[k] = hsq2_rn(e, nzh2);
     } else {
@@ -216,7 +222,7 @@ __device__ __forceinline__ float candidate_f16(const float x[16], const uint32_t
 union Tables {
   struct {
     float inv[2][256];         // 1 / (S * gs) per tensor
-    uint32_t neg_sg2[2][256];  // (-RN16(S * RN16(gs))) in both halves, per tensor
+    uint32_t S2[256];          // (S, S) as half2 (binary16-error recipes)
   } split;                     // standard NVFP4 and the binary16-error recipes
   uint2 pair[2][256];          // binary32-error recipes: (bits of 1 / (S * gs), (S, S) as half2)
 };
@@ -272,10 +278,10 @@ __device__ __forceinline__ BlockOut quantize_block(const U32x8& in, const Tensor
 #pragma unroll
     for (int k = 0; k < 8; ++k) xh[k] = BF16 ? f16x2_from_f32(x[2 * k], x[2 * k + 1]) : in.w[k];
     const uint32_t nzh2 = (nz >> 16) | nz;  // binary16 -0 in both halves
-    ea = candidate_f16<MODE == 4>(x, xh, tab.split.inv[kv][sa], tab.split.neg_sg2[kv][sa], nzh2,
-                                  a0, a1);
-    eb = candidate_f16<MODE == 4>(x, xh, tab.split.inv[kv][sb], tab.split.neg_sg2[kv][sb], nzh2,
-                                  b0, b1);
+    ea = candidate_f16<MODE == 4>(x, xh, tab.split.inv[kv][sa], tab.split.S2[sa], tc.neg_gh2,
+                                  nzh2, a0, a1);
+    eb = candidate_f16<MODE == 4>(x, xh, tab.split.inv[kv][sb], tab.split.S2[sb], tc.neg_gh2,
+                                  nzh2, b0, b1);
   }
   const bool take_b = eb < ea;
   r.c0 = take_b ? b0 : a0;
@@ -314,12 +320,8 @@ __device__ __forceinline__ void fill_tables(Tables& tab, const float gs[2]) {
       if (MODE == 1 || MODE == 2) {
         tab.pair[kv][s] = make_uint2(__float_as_uint(inv), S2);
       } else {
-        const __half gh = __float2half_rn(gs[kv]);
-        const __half sg =
-            __hmul_rn(__ushort_as_half(static_cast<unsigned short>(S2 & 0xFFFFu)), gh);
-        const uint32_t n = static_cast<uint32_t>(__half_as_ushort(sg)) ^ 0x8000u;
         tab.split.inv[kv][s] = inv;
-        tab.split.neg_sg2[kv][s] = n | (n << 16);
+        if (kv == 0) tab.split.S2[s] = S2;
       }
     }
   }
@@ -690,8 +692,9 @@ nvfp4_status launch_tma(const AppendArgs& a, uint32_t row_bytes, uint32_t nkv,
   int ns = static_cast<int>(100u * 1024u / one);
   ns = ns < 2 ? 2 : (ns > 6 ? 6 : ns);
   const AppendTmaLayout L = append_tma_layout(rows, row_bytes, nkv, ns);
-  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       static_cast<int>(L.total));
+  const nvfp4_status st = set_dynamic_smem(reinterpret_cast<const void*>(kern), L.total,
+                                           "nvfp4_quantize_append_paged");
+  if (st != NVFP4_OK) return st;
   const int64_t tiles = (a.nnz + rows - 1) / rows;
   const int64_t cap = static_cast<int64_t>(sm_count()) *
                       blocks_per_sm(reinterpret_cast<const void*>(kern), append_threads(MODE),

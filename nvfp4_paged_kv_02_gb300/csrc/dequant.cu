@@ -344,8 +344,9 @@ nvfp4_status launch_t(const DequantArgs& a, cudaStream_t stream) {
   const auto kern = dequant_kernel<OUT_BF16, BT64, VEC256>;
   const size_t smem = static_cast<size_t>(a.B) * sizeof(int32_t);
   if (smem > 48 * 1024) {
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(smem));
+    const nvfp4_status st =
+        set_dynamic_smem(reinterpret_cast<const void*>(kern), smem, "nvfp4_dequantize_paged");
+    if (st != NVFP4_OK) return st;
   }
   const int grid = sm_count() * blocks_per_sm(reinterpret_cast<const void*>(kern), kThreads, smem);
   kern<<<grid, kThreads, smem, stream>>>(a);
@@ -366,8 +367,9 @@ nvfp4_status launch_tma(const DequantArgs& a, uint32_t codes_bytes, uint32_t sf_
                         cudaStream_t stream) {
   const auto kern = dequant_tma_kernel<OUT_BF16, BT64>;
   const TmaLayout L = tma_layout(a.B, codes_bytes, sf_bytes, stages_for(codes_bytes, sf_bytes, 48u * 1024u));
-  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       static_cast<int>(L.total));
+  const nvfp4_status st =
+      set_dynamic_smem(reinterpret_cast<const void*>(kern), L.total, "nvfp4_dequantize_paged");
+  if (st != NVFP4_OK) return st;
   const int grid =
       sm_count() * blocks_per_sm(reinterpret_cast<const void*>(kern), kTmaThreads, L.total);
   kern<<<grid, kTmaThreads, L.total, stream>>>(a, L);

@@ -20,6 +20,9 @@ void clear_error();
 nvfp4_status fail(nvfp4_status code, const std::string& msg);
 // Check the launch that was just enqueued.
 nvfp4_status check_launch(const char* what);
+// Opt `kernel` in to `bytes` of dynamic shared memory; a refusal is reported as
+// NVFP4_ERR_CUDA with the byte count (the launch would otherwise fail without the cause).
+nvfp4_status set_dynamic_smem(const void* kernel, size_t bytes, const char* what);
 
 // Streaming multiprocessors of the current device.
 int sm_count();
@@ -119,6 +122,20 @@ struct MaterializeArgs {
   int32_t* status;
 };
 nvfp4_status launch_materialize(const MaterializeArgs& a, cudaStream_t stream);
+
+// A materialize launch configuration chosen once (the prepared form).
+struct MaterializeLaunch {
+  int32_t bulk;   // 1: the bulk-copy ring, 0: the direct-load kernel
+  int32_t max_B;  // requests the shared-memory scan has room for
+  int32_t smem;   // dynamic shared memory bytes
+  int32_t grid;   // CTAs
+};
+// Choose the kernel and its launch shape for pages of cb code bytes and sb scale bytes and
+// up to max_B requests; opts the kernel in to its shared memory.
+nvfp4_status prepare_materialize(bool bulk, bool v_interleaved, int max_B, int64_t cb,
+                                 int64_t sb, MaterializeLaunch* out);
+nvfp4_status launch_materialize_prepared(const MaterializeArgs& a, const MaterializeLaunch& c,
+                                         cudaStream_t stream);
 
 // ---- global scale ------------------------------------------------------------------------
 nvfp4_status launch_global_scale(const void* x, bool bf16, int64_t numel, float denom,

@@ -330,7 +330,55 @@ __global__ void __launch_bounds__(kTmaThreads, 3) materialize_tma_kernel(const M
   }
 }
 
+const void* materialize_kernel_ptr(bool bulk, bool v_interleaved) {
+  if (bulk)
+    return v_interleaved ? reinterpret_cast<const void*>(materialize_tma_kernel<true>)
+                         : reinterpret_cast<const void*>(materialize_tma_kernel<false>);
+  return v_interleaved ? reinterpret_cast<const void*>(materialize_kernel<true>)
+                       : reinterpret_cast<const void*>(materialize_kernel<false>);
+}
+
+// Dynamic shared memory of a launch for up to max_B requests.
+size_t materialize_smem(bool bulk, int max_B, int64_t cb, int64_t sb) {
+  if (!bulk) return static_cast<size_t>(max_B) * sizeof(int32_t);
+  return tma_layout(max_B, static_cast<uint32_t>(cb), static_cast<uint32_t>(sb),
+                    stages_for(static_cast<uint32_t>(cb), static_cast<uint32_t>(sb)))
+      .total;
+}
+
 }  // namespace
+
+nvfp4_status prepare_materialize(bool bulk, bool v_interleaved, int max_B, int64_t cb,
+                                 int64_t sb, MaterializeLaunch* out) {
+  const void* kern = materialize_kernel_ptr(bulk, v_interleaved);
+  const size_t smem = materialize_smem(bulk, max_B, cb, sb);
+  if (bulk || smem > 48 * 1024) {
+    const nvfp4_status st = set_dynamic_smem(kern, smem, "nvfp4_materializer_prepare");
+    if (st != NVFP4_OK) return st;
+  }
+  const int threads = bulk ? kTmaThreads : kThreads;
+  out->bulk = bulk ? 1 : 0;
+  out->max_B = max_B;
+  out->smem = static_cast<int32_t>(smem);
+  out->grid = sm_count() * blocks_per_sm(kern, threads, smem);
+  return NVFP4_OK;
+}
+
+nvfp4_status launch_materialize_prepared(const MaterializeArgs& a, const MaterializeLaunch& c,
+                                         cudaStream_t stream) {
+  if (c.bulk) {
+    const int64_t cb = static_cast<int64_t>(a.ps) * a.H * (a.D / 2);
+    const int64_t sb = static_cast<int64_t>(a.ps) * a.H * (a.D / 16);
+    const TmaLayout L = tma_layout(c.max_B, static_cast<uint32_t>(cb), static_cast<uint32_t>(sb),
+                                   stages_for(static_cast<uint32_t>(cb), static_cast<uint32_t>(sb)));
+    if (a.v_interleaved) materialize_tma_kernel<true><<<c.grid, kTmaThreads, c.smem, stream>>>(a, L);
+    else materialize_tma_kernel<false><<<c.grid, kTmaThreads, c.smem, stream>>>(a, L);
+  } else {
+    if (a.v_interleaved) materialize_kernel<true><<<c.grid, kThreads, c.smem, stream>>>(a);
+    else materialize_kernel<false><<<c.grid, kThreads, c.smem, stream>>>(a);
+  }
+  return check_launch("nvfp4_materializer_run");
+}
 
 nvfp4_status launch_materialize(const MaterializeArgs& a, cudaStream_t stream) {
   const int64_t cb = static_cast<int64_t>(a.ps) * a.H * (a.D / 2);
@@ -339,8 +387,9 @@ nvfp4_status launch_materialize(const MaterializeArgs& a, cudaStream_t stream) {
     const auto kern = a.v_interleaved ? materialize_tma_kernel<true> : materialize_tma_kernel<false>;
     const TmaLayout L = tma_layout(a.B, static_cast<uint32_t>(cb), static_cast<uint32_t>(sb),
                                    stages_for(static_cast<uint32_t>(cb), static_cast<uint32_t>(sb)));
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(L.total));
+    const nvfp4_status st =
+        set_dynamic_smem(reinterpret_cast<const void*>(kern), L.total, "nvfp4_materialize_fp8");
+    if (st != NVFP4_OK) return st;
     const int grid =
         sm_count() * blocks_per_sm(reinterpret_cast<const void*>(kern), kTmaThreads, L.total);
     kern<<<grid, kTmaThreads, L.total, stream>>>(a, L);
@@ -349,8 +398,9 @@ nvfp4_status launch_materialize(const MaterializeArgs& a, cudaStream_t stream) {
   const auto kern = a.v_interleaved ? materialize_kernel<true> : materialize_kernel<false>;
   const size_t smem = static_cast<size_t>(a.B) * sizeof(int32_t);
   if (smem > 48 * 1024) {
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(smem));
+    const nvfp4_status st =
+        set_dynamic_smem(reinterpret_cast<const void*>(kern), smem, "nvfp4_materialize_fp8");
+    if (st != NVFP4_OK) return st;
   }
   const int grid = sm_count() * blocks_per_sm(reinterpret_cast<const void*>(kern), kThreads, smem);
   kern<<<grid, kThreads, smem, stream>>>(a);

@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_e4m3_max(lib):
-    assert lib.nvfp4_abi_version() == 2
+    assert lib.nvfp4_abi_version() == 3
     assert nv.nvfp4_e4m3_max(None) == 448.0
     assert nv.nvfp4_e4m3_max(nv.NVFP44Over6Config(256.0, "MSE")) == 256.0
 
@@ -172,6 +172,41 @@ def materialize(lib, **kw):
 def test_materialize_rejects(lib, kw, code, text):
     assert materialize(lib, **kw) == code
     assert text in err(lib)
+
+
+@pytest.mark.parametrize("kw,code,text", [
+    (dict(D=96), nv.ERR_INVALID_ARG, "divisible by 64"),
+    (dict(ps=6), nv.ERR_INVALID_ARG, "divisible by 4"),
+    (dict(maxb=0), nv.ERR_INVALID_ARG, "max_batch_size"),
+    (dict(maxb=20000), nv.ERR_INVALID_ARG, "max_batch_size"),
+    (dict(dps=16 * 8 * 64 - 16), nv.ERR_INVALID_ARG, "smaller than a page"),
+    (dict(dps=16 * 8 * 64 + 8), nv.ERR_ALIGNMENT, "multiple of 16"),
+    (dict(sps=16 * 8 * 8 + 1), nv.ERR_ALIGNMENT, "even"),
+    (dict(vsf=2), nv.ERR_INVALID_ARG, "v_scale_layout"),
+    (dict(vsf=nv.SF_INTERLEAVED4, layout=0), nv.ERR_UNSUPPORTED, "HND pages only"),
+])
+def test_materializer_prepare_rejects(lib, kw, code, text):
+    a = dict(ps=16, H=8, D=128, layout=1, shared=1, vsf=nv.SF_LINEAR, dps=16 * 8 * 64,
+             sps=16 * 8 * 8, maxb=64)
+    a.update(kw)
+    m = nv._Materializer()
+    m.magic = 123
+    assert lib.nvfp4_materializer_prepare(ctypes.byref(m), a["ps"], a["H"], a["D"], a["layout"],
+                                          a["shared"], a["vsf"], a["dps"], a["sps"],
+                                          a["maxb"]) == code
+    assert text in err(lib)
+    assert m.magic == 0  # a failed prepare leaves the struct unusable
+
+
+def test_materializer_run_needs_a_prepared_struct(lib):
+    m = nv._Materializer()
+    assert lib.nvfp4_materializer_run(
+        ctypes.byref(m), cache(), cache(), ctypes.c_void_p(FAKE), 4, ctypes.c_void_p(FAKE), 2, 4,
+        None, -1, ctypes.c_void_p(FAKE), 9, ctypes.c_void_p(FAKE), None, None) == nv.ERR_INVALID_ARG
+    assert "not prepared" in err(lib)
+    assert lib.nvfp4_materializer_run(
+        None, cache(), cache(), ctypes.c_void_p(FAKE), 4, ctypes.c_void_p(FAKE), 2, 4, None, -1,
+        ctypes.c_void_p(FAKE), 9, ctypes.c_void_p(FAKE), None, None) == nv.ERR_INVALID_ARG
 
 
 def test_materializer_interleaved_needs_hnd():

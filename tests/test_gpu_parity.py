@@ -123,31 +123,37 @@ def test_materialize_run_form_and_workspace():
     assert (g.fp8[-3:] == PL.SENT_FP8).all()
 
 
-def test_materializer_class_matches_functional():
+@pytest.mark.parametrize("shared", [True, False])
+def test_materializer_class_matches_oracle(shared):
+    """NVFP4KVMaterializer.run() (the prepared C form) against the oracle's materialize with
+    run() semantics (only active table entries written), on caches the oracle appended; then
+    the same run captured in a CUDA graph and replayed after new lengths are copied into the
+    captured tensor, against the oracle on those lengths."""
     import nvfp4_paged_kv_02_gb300 as nv
-    w = W.random_case(401, B=4, H=8, D=128, ps=16, layout=W.HND, dtype=torch.bfloat16,
-                      max_len=100, compact_indptr=True)
+    w = W.random_case(401 + int(shared), B=4, H=8, D=128, ps=16, layout=W.HND,
+                      dtype=torch.bfloat16, max_len=100, compact_indptr=True, mat_shared=shared)
     dev = torch.device("cuda")
-    r = PL.run_gpu(w, do_dequant=False)
+    o = PL.run_oracle(w, do_dequant=False, extra_out_pages=2, zero_tables=False)
     dps, sps = PL.strides(w)
-    kd = torch.from_numpy(r.k_data).to(dev).view(w.num_pages, w.H, w.ps, w.D // 2)
-    ks = torch.from_numpy(r.k_sf).to(dev).view(w.num_pages, w.H, w.ps, w.D // 16)
-    vd = torch.from_numpy(r.v_data).to(dev).view(w.num_pages, w.H, w.ps, w.D // 2)
-    vs = torch.from_numpy(r.v_sf).to(dev).view(w.num_pages, w.H, w.ps, w.D // 16)
-    t = lambda a: torch.as_tensor(a).to(dev)
-    m = nv.NVFP4KVMaterializer(w.H, w.ps, w.D, dev)
+    kc = O.PagedCache(o.k_data, o.k_sf, dps, sps)
+    vc = O.PagedCache(o.v_data, o.v_sf, dps, sps)
+    kd, ks = PL.hnd_views(w, kc, dev)
+    vd, vs = PL.hnd_views(w, vc, dev)
+    t = lambda a: torch.as_tensor(np.ascontiguousarray(a)).to(dev)
+    m = nv.NVFP4KVMaterializer(w.H, w.ps, w.D, dev, uses_shared_paged_kv_idx=shared)
     n_out, mpps = PL.mat_shape(w)
-    out = torch.full((n_out + 2, 2, w.H, w.ps, w.D), 0x5A, dtype=torch.uint8,
+    out = torch.full((n_out + 2, 2, w.H, w.ps, w.D), PL.SENT_FP8, dtype=torch.uint8,
                      device=dev).view(torch.float8_e4m3fn)
-    tbl = torch.zeros((w.B, mpps), dtype=torch.int32, device=dev)
-    m.run(kd, vd, ks, vs, t(w.mat_block_tables), t(w.seq_lens), t(w.kv_page_indptr), out=out,
-          fp8_block_tables=tbl)
-    got = out.view(torch.uint8).cpu().numpy()
-    assert np.array_equal(got[:n_out], r.fp8)
-    assert np.array_equal(tbl.cpu().numpy(), r.tables)
-    # graph capture of run(): replay after new lengths are copied into the captured tensors
-    sl = t(w.seq_lens).clone()
-    bt, ip = t(w.mat_block_tables), t(w.kv_page_indptr)
+    tbl = torch.full((w.B, mpps), PL.SENT_TABLE, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    bt, sl, ip = t(w.mat_block_tables), t(w.seq_lens), t(w.kv_page_indptr)
+    m.run(kd, vd, ks, vs, bt, sl, ip, out=out, fp8_block_tables=tbl, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(out.view(torch.uint8).cpu().numpy(), o.fp8)
+    assert np.array_equal(tbl.cpu().numpy(), o.tables)
+    # graph capture of run(): replay after shorter lengths are copied into the captured
+    # tensor (same page reservations), compared with the oracle on those lengths
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         m.run(kd, vd, ks, vs, bt, sl, ip, out=out, fp8_block_tables=tbl)
@@ -155,10 +161,18 @@ def test_materializer_class_matches_functional():
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         m.run(kd, vd, ks, vs, bt, sl, ip, out=out, fp8_block_tables=tbl)
-    out.view(torch.uint8).fill_(0x5A)
+    shorter = np.maximum(w.seq_lens - 17, 1).astype(np.int32)
+    sl.copy_(torch.from_numpy(shorter))
+    out.view(torch.uint8).fill_(PL.SENT_FP8)
+    tbl.fill_(PL.SENT_TABLE)
     graph.replay()
     torch.cuda.synchronize()
-    assert np.array_equal(out.view(torch.uint8).cpu().numpy()[:n_out], r.fp8)
+    want = np.full_like(o.fp8, PL.SENT_FP8)
+    want_tbl = np.full_like(o.tables, PL.SENT_TABLE)
+    O.materialize_fp8(kc, vc, w.ps, w.H, w.D, W.HND, w.mat_block_tables, shared, shorter,
+                      w.max_kv_len, w.kv_page_indptr, want, want_tbl, False, 0)
+    assert np.array_equal(out.view(torch.uint8).cpu().numpy(), want)
+    assert np.array_equal(tbl.cpu().numpy(), want_tbl)
 
 
 def test_codec_edge_values():
