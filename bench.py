@@ -143,6 +143,8 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
+    INTERVAL_MS = 20
+
     def __init__(self, out_path: str):
         self.path = out_path
         self.proc = None
@@ -152,7 +154,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "-lms", str(self.INTERVAL_MS)], stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
 
@@ -176,10 +178,12 @@ class ClockSampler:
                 if len(parts) < 10:
                     continue
                 try:
-                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    whole, _, frac = parts[0].partition(".")
+                    ts = time.mktime(time.strptime(whole, "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + frac) if frac.isdigit() else 0.0
                 except ValueError:
                     continue
-                if not (t0 - 1.0 <= ts <= t1):
+                if not (t0 - 0.05 <= ts <= t1 + 0.05):
                     continue
                 parts = parts[1:]
                 if want is not None and want.isdigit() and parts[0] != want:
@@ -195,7 +199,8 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "interval_ms": self.INTERVAL_MS, "window_s": round(t1 - t0, 3)}
 
 
 # ---------------------------------------------------------------------------------------
@@ -398,6 +403,131 @@ def active_pages(w: W.Workload) -> int:
 
 
 # ---------------------------------------------------------------------------------------
+# the other configurations, measured after the headline step
+# ---------------------------------------------------------------------------------------
+
+SECONDARY = ("decode", "prefill", "materialize", "contig")
+
+
+def time_ops(step, dev: torch.device, n_steps: int, warmup: int = 3):
+    """Mean device time (ms) per op of `step` over n_steps timed steps after `warmup`
+    untimed ones. When every op moves under 1 GB, L2 is flushed before each op (256 MB
+    written, then 256 MB read), outside the op's events."""
+    nbytes, _ = step.op_bytes()
+    small = max(nbytes.values()) < 1e9
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if small else None
+    flush_read = torch.zeros(256 << 20, dtype=torch.uint8, device=dev) if small else None
+    count = [0]
+
+    def flush_l2():
+        count[0] += 1
+        flush.fill_(count[0] & 0xFF)
+        flush_read.sum()
+
+    for _ in range(warmup):
+        step.run()
+    n_ops = len(step.NAMES)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * n_ops)]
+           for _ in range(n_steps)]
+    torch.cuda.synchronize(dev)
+    for s in range(n_steps):
+        step.run(evs[s], flush_l2 if small else None)
+    torch.cuda.synchronize(dev)
+    op_ms = {k: float(np.mean([evs[s][2 * i].elapsed_time(evs[s][2 * i + 1])
+                               for s in range(n_steps)]))
+             for i, k in enumerate(step.NAMES)}
+    return op_ms, small
+
+
+def op_table(step, op_ms, peak: float):
+    nbytes, ntok = step.op_bytes()
+    out = {}
+    for k, ms in op_ms.items():
+        gbs = nbytes[k] / (ms * 1e-3) / 1e9
+        out[k] = {"us": ms * 1e3, "bytes": nbytes[k], "GB_s": gbs,
+                  "pct_of_8TBs": 100 * gbs / NOMINAL_HBM_GBS,
+                  "pct_of_measured_copy": 100 * gbs / peak,
+                  "tokens_per_s": ntok[k] / (ms * 1e-3)}
+    return out
+
+
+def materialize_host_cost(step, n_calls: int = 200, layers: int = 32):
+    """Host time per call (CPU clock, microseconds) of issuing the materialize three ways on
+    the materialize workload ("NVFP4KVMaterializer": the functional call validates every
+    tensor and allocates the block table each time, the class validates once): the
+    functional nvfp4_materialize_fp8 (allocating its outputs), NVFP4KVMaterializer.run()
+    with caller-owned outputs, and one replay of a CUDA graph holding `layers` run() calls,
+    per layer. Only the enqueueing is timed; the device work drains outside the timer."""
+    nv, w, dev = step.nv, step.w, step.dev
+    lay = step.lay
+    kd, vd = step.cache
+    ks, vs = step.sf
+    args = (kd, vd, ks, vs, step.mat_bt, step.seq_lens)
+
+    def per_call(fn, n):
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(n):
+            fn()
+        t1 = time.perf_counter()
+        torch.cuda.synchronize(dev)
+        return (t1 - t0) / n * 1e6
+
+    def functional():
+        nv.nvfp4_materialize_fp8(*args, w.max_kv_len, w.mat_shared, None, step.indptr,
+                                 w.mat_num_pages, lay)
+
+    m = nv.NVFP4KVMaterializer(w.H, w.ps, w.D, dev, uses_shared_paged_kv_idx=w.mat_shared,
+                               kv_layout=lay, max_batch_size=w.B)
+    out, tables = step.fp8, step.tables
+
+    def run():
+        m.run(*args, step.indptr, out=out, fp8_block_tables=tables)
+
+    for fn in (functional, run):  # warm-up: first-call set-up, allocator, prepared shapes
+        fn()
+        fn()
+    res = {"functional_us": per_call(functional, n_calls), "materializer_run_us": per_call(run, n_calls)}
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        run()
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(layers):
+            run()
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    res["graph_replay_us_per_layer"] = per_call(graph.replay, max(4, n_calls // layers)) / layers
+    res["graph_layers"] = layers
+    res["calls"] = n_calls
+    return res
+
+
+def measure_configs(w_large: W.Workload, dev: torch.device, n_steps: int = 20):
+    """Per-op figures of the decode, prefill and materialize workloads and of the contiguous
+    form (on the large pool's K and V rows), each timed on its own after the headline step."""
+    peak, _ = measured_peaks()
+    out = {}
+    for name in SECONDARY:
+        w = w_large if name == "contig" else make_workload(name, dev)
+        step = ContigStep(w, dev) if name == "contig" else Step(w, dev)
+        op_ms, small = time_ops(step, dev, n_steps)
+        status = int(step.status.item())
+        host = materialize_host_cost(step) if name == "materialize" else None
+        out[name] = {"config": step.config(), "steps": n_steps,
+                     "l2": "flushed before every op" if small else "inputs larger than L2",
+                     "ops": op_table(step, op_ms, peak), "device_status": status,
+                     "gpu_launches": step.launches_per_step * n_steps}
+        if host is not None:
+            out[name]["host_cost"] = host
+        del step
+        torch.cuda.empty_cache()
+    return out
+
+
+# ---------------------------------------------------------------------------------------
 # the CPU oracle on a bounded sample (baseline and reference arm)
 # ---------------------------------------------------------------------------------------
 
@@ -551,6 +681,8 @@ def main():
                     help="large_pool: pool size (K+V codes and scales), GB")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="large_pool: skip timing the other configurations afterwards")
     ap.add_argument("--v-scales", default="linear", choices=["linear", "interleaved4"],
                     help="layout of the V block scales the materialize reads (HND workloads)")
     args = ap.parse_args()
@@ -655,6 +787,13 @@ def main():
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w) if isinstance(step, Step) else cpu_baseline_contig(w)
+    configs = None
+    if rank == 0 and args.workload == "large_pool" and not args.no_configs:
+        cfg_main = step.config()
+        launches = step.launches_per_step
+        del step  # frees the pool and the outputs before the other workloads run
+        torch.cuda.empty_cache()
+        configs = measure_configs(w, dev)
 
     if rank == 0:
         line = {
@@ -663,7 +802,7 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": arith_dtype(w),
             "data": "synthetic",
-            "config": {**step.config(),
+            "config": {**(cfg_main if configs is not None else step.config()),
                        "l2": "flushed before every op (256 MB write, then 256 MB read), "
                              "outside the timed ops" if small
                        else "inputs larger than L2 (129 MB); no flush",
@@ -674,9 +813,12 @@ def main():
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": nbytes[dom] / (op_ms[dom] * 1e-3) / 1e9 / peak,
                          "traffic": traffic_per_launch(dom, ntok[dom])},
-            "clocks": clk, "gpu_launches": step.launches_per_step * args.steps,
+            "clocks": clk,
+            "gpu_launches": (launches if configs is not None else step.launches_per_step)
+            * args.steps,
             "e2e": e2e, "cpu_baseline": cpu, "device_status": status,
             "diagnostics": diag,
+            "configs": configs,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -690,10 +832,16 @@ def measure_e2e(step, w: W.Workload, args, total_bytes: int, world: int):
     step's summary (the two global scales and the device status word). Steps are pipelined
     the way a serving loop would run them: the copies of step i+1 (on a copy stream, into
     the other of two device input buffers) overlap the compute of step i; a buffer is
-    refilled only after the step that read it has finished."""
+    refilled only after the step that read it has finished.
+
+    The paged cache, the dequantized K/V and the FP8 copy stay on the device, as a serving
+    loop keeps them. A second figure also reads the dequantized rows of every request back
+    to pinned host memory each step (on a third stream; the next step's compute waits until
+    that read is done, since it rewrites the same outputs)."""
     dev = step.dev
     comp = torch.cuda.current_stream(dev)
     copy = torch.cuda.Stream(dev)
+    back = torch.cuda.Stream(dev)
     hk = torch.empty(step.k.shape, dtype=step.k.dtype, pin_memory=True)
     hv = torch.empty(step.v.shape, dtype=step.v.dtype, pin_memory=True)
     hk.copy_(step.k)
@@ -703,10 +851,15 @@ def measure_e2e(step, w: W.Workload, args, total_bytes: int, world: int):
     summary = [torch.empty(3, dtype=torch.float32, device=dev) for _ in range(2)]
     copied = [torch.cuda.Event() for _ in range(2)]
     done = [torch.cuda.Event() for _ in range(2)]
+    read_done = torch.cuda.Event()
     for e in done:
         e.record(comp)
+    read_done.record(comp)
+    lens = np.minimum(w.seq_lens.astype(np.int64), w.max_seq_len)
+    rows = [(b, int(n)) for b, n in enumerate(lens) if n > 0]
+    out_host = None
 
-    def one(i):
+    def one(i, readback=False):
         b = i % 2
         k, v = bufs[b]
         with torch.cuda.stream(copy):
@@ -715,6 +868,8 @@ def measure_e2e(step, w: W.Workload, args, total_bytes: int, world: int):
             v.copy_(hv, non_blocking=True)
             copied[b].record(copy)
         comp.wait_event(copied[b])
+        if readback:
+            comp.wait_event(read_done)  # the previous step's outputs have been read back
         step.k, step.v = k, v
         step.run()
         sm = summary[b]
@@ -723,38 +878,78 @@ def measure_e2e(step, w: W.Workload, args, total_bytes: int, world: int):
         sm[2] = step.status[0].float()
         res[b].copy_(sm, non_blocking=True)
         done[b].record(comp)
+        if readback:
+            back.wait_stream(comp)
+            with torch.cuda.stream(back):
+                for r, n in rows:
+                    out_host[0][r, :n].copy_(step.out_k[r, :n], non_blocking=True)
+                    out_host[1][r, :n].copy_(step.out_v[r, :n], non_blocking=True)
+                read_done.record(back)
 
-    for i in range(2):
-        one(i)
-    torch.cuda.synchronize(dev)
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    # three timed windows of n steps; the median window is reported (the host link is shared
-    # with the rest of the machine, and one window can land on a burst of other traffic)
-    n = max(4, min(args.steps, 6))
-    windows = []
-    for _ in range(3):
-        a.record(comp)
-        copy.wait_stream(comp)  # the timed copies start after the start event
-        for i in range(n):
-            one(i)
-        comp.wait_stream(copy)
-        b.record(comp)
+    def windows(readback=False):
+        for i in range(2):
+            one(i, readback)
         torch.cuda.synchronize(dev)
-        windows.append(a.elapsed_time(b) / n)
-    step.k, step.v = bufs[0]
-    ms = max_over_ranks(float(np.median(windows)), dev)
+        a = torch.cuda.Event(enable_timing=True)
+        z = torch.cuda.Event(enable_timing=True)
+        # three timed windows of n steps; the median window is reported (the host link is
+        # shared with the rest of the machine, and one window can land on a burst of other
+        # traffic)
+        n = max(4, min(args.steps, 6))
+        out = []
+        for _ in range(3):
+            a.record(comp)
+            copy.wait_stream(comp)  # the timed copies start after the start event
+            for i in range(n):
+                one(i, readback)
+            comp.wait_stream(copy)
+            comp.wait_stream(back)
+            z.record(comp)
+            torch.cuda.synchronize(dev)
+            out.append(a.elapsed_time(z) / n)
+        return out
+
+    fd, clock_path = tempfile.mkstemp(prefix="nvfp4kv_clocks_e2e_", suffix=".csv")
+    os.close(fd)
+    clocks = ClockSampler(clock_path)
+    clocks.start()
+    time.sleep(0.3)
+    h0 = time.time()
+    wins = windows()
+    h1 = time.time()
+    clk = clocks.stop(h0, h1)
+    ms = max_over_ranks(float(np.median(wins)), dev)
     h2d = hk.numel() * hk.element_size() + hv.numel() * hv.element_size()
     # the host link alone: one copy of the K rows, for reading the e2e figure against
+    a = torch.cuda.Event(enable_timing=True)
+    z = torch.cuda.Event(enable_timing=True)
     a.record(comp)
     bufs[1][0].copy_(hk, non_blocking=True)
-    b.record(comp)
+    z.record(comp)
     torch.cuda.synchronize(dev)
-    link = hk.numel() * hk.element_size() / (a.elapsed_time(b) * 1e-3) / 1e9
+    link = hk.numel() * hk.element_size() / (a.elapsed_time(z) * 1e-3) / 1e9
+
+    out_host = tuple(torch.empty(step.out_k.shape, dtype=step.out_k.dtype, pin_memory=True)
+                     for _ in range(2))
+    wins_rb = windows(readback=True)
+    ms_rb = max_over_ranks(float(np.median(wins_rb)), dev)
+    d2h_rb = 2 * int(lens.sum()) * w.H * w.D * step.out_k.element_size() + 12
+    step.k, step.v = bufs[0]
     return {"value": world * total_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 12, "ms_per_step": ms,
+            "value_counts": "appended K/V rows copied in, the step's summary (two global "
+                            "scales and the status word) read back",
+            "resident_on_device": ["paged K/V cache (codes and block scales)",
+                                   "dequantized K/V (out_k, out_v)",
+                                   "FP8 copy and fp8_block_tables"],
             "pipelined": "copies of step i+1 overlap the compute of step i (two buffers)",
-            "windows_ms_per_step": windows, "host_to_device_gbs": link}
+            "windows_ms_per_step": wins, "host_to_device_gbs": link, "clocks": clk,
+            "with_dequant_readback": {
+                "value": world * total_bytes / (ms_rb * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": ms_rb, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h_rb,
+                "reads_back": "every request's dequantized K and V rows (rows < seq_lens) and "
+                              "the summary",
+                "windows_ms_per_step": wins_rb}}
 
 
 if __name__ == "__main__":
