@@ -116,9 +116,10 @@ def source_hash(op: str) -> str:
 
 
 def traffic_per_launch(op: str, units: int):
-    """DRAM bytes (read + write) per launch of the op's kernel: the bytes per unit that an ncu
-    capture measured, times the units of this launch. None when there is no capture or the
-    kernel's sources changed since it was taken."""
+    """DRAM bytes (read + write) per launch of the op's kernel, from ncu captures of the same
+    kernel at two sizes: traffic = marginal bytes per unit * units + bytes at zero units (the
+    second is negative: output lines still dirty in L2 when the kernel ends, written back
+    later). None when there is no capture or the kernel's sources changed since."""
     want = source_hash(op)
     for path in TRAFFIC_FILES:
         if not os.path.exists(path):
@@ -126,9 +127,9 @@ def traffic_per_launch(op: str, units: int):
         with open(path) as f:
             for ln in f:
                 cells = [c.strip().strip("`") for c in ln.strip().strip("|").split("|")]
-                if len(cells) >= 6 and cells[0] == op and cells[1] == want:
+                if len(cells) >= 12 and cells[0] == op and cells[1] == want:
                     try:
-                        return float(cells[5]) * units
+                        return float(cells[8]) * units + float(cells[9])
                     except ValueError:
                         return None
     return None
@@ -452,11 +453,12 @@ def op_table(step, op_ms, peak: float):
 
 
 def materialize_host_cost(step, n_calls: int = 200, layers: int = 32):
-    """Host time per call (CPU clock, microseconds) of issuing the materialize three ways on
+    """Host time per call (CPU clock, microseconds) of issuing the materialize four ways on
     the materialize workload ("NVFP4KVMaterializer": the functional call validates every
     tensor and allocates the block table each time, the class validates once): the
     functional nvfp4_materialize_fp8 (allocating its outputs), NVFP4KVMaterializer.run()
-    with caller-owned outputs, and one replay of a CUDA graph holding `layers` run() calls,
+    with caller-owned outputs, the prepared C entry point called through ctypes with its
+    arguments marshalled once, and one replay of a CUDA graph holding `layers` run() calls,
     per layer. Only the enqueueing is timed; the device work drains outside the timer."""
     nv, w, dev = step.nv, step.w, step.dev
     lay = step.lay
@@ -484,10 +486,26 @@ def materialize_host_cost(step, n_calls: int = 200, layers: int = 32):
     def run():
         m.run(*args, step.indptr, out=out, fp8_block_tables=tables)
 
-    for fn in (functional, run):  # warm-up: first-call set-up, allocator, prepared shapes
+    # the C entry point alone, its arguments marshalled once (ctypes call overhead included)
+    import ctypes
+    L = nv.load()
+    kc, vc = nv._one_cache(kd, ks), nv._one_cache(vd, vs)
+    prepared = m._prepare(kc.data_page_stride, kc.sf_page_stride, m._max_batch)
+    vp = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    c_args = (ctypes.byref(prepared), kc._c(), vc._c(), vp(step.mat_bt), step.mat_bt.shape[-1],
+              vp(step.seq_lens), tables.shape[0], tables.shape[1], vp(step.indptr),
+              out.shape[0] - 1, vp(out), out.shape[0], vp(tables), None,
+              *nv._ws_stream(dev))
+
+    def c_run():
+        if L.nvfp4_materializer_run(*c_args) != 0:
+            raise RuntimeError("nvfp4_materializer_run failed")
+
+    for fn in (functional, run, c_run):  # warm-up: first-call set-up, allocator, shapes
         fn()
         fn()
-    res = {"functional_us": per_call(functional, n_calls), "materializer_run_us": per_call(run, n_calls)}
+    res = {"functional_us": per_call(functional, n_calls), "materializer_run_us": per_call(run, n_calls),
+           "c_abi_run_us": per_call(c_run, n_calls)}
     s = torch.cuda.Stream(dev)
     s.wait_stream(torch.cuda.current_stream(dev))
     with torch.cuda.stream(s):

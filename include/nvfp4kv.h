@@ -36,6 +36,15 @@
  *     or page whose device-held index falls outside them is skipped; if `dev_status` is not
  *     NULL the kernel ORs the matching NVFP4_DEV_* bit into *dev_status (device memory,
  *     one int32 the caller zeroes).
+ *   - Work distribution (`workspace`, the last-but-one argument of the append, dequantize,
+ *     materialize and contiguous-quantize calls): NULL, or NVFP4_WORKSPACE_BYTES of device
+ *     memory, 8-byte aligned, that is zero before its first use. With it, the persistent
+ *     CTAs of the bulk-copy kernels take work items from a counter there as they free up
+ *     (CTAs on SMs that run ahead take more); the kernel sets it back to zero before it
+ *     finishes, so the same workspace serves the next call. Without it each CTA takes a
+ *     fixed share. The results are the same either way. One workspace serves one call at a
+ *     time: calls that may run at the same time on the device (different streams, or a
+ *     graph replayed beside direct calls) need different workspaces.
  *   - Launch errors are returned as NVFP4_ERR_CUDA with the CUDA error text.
  *   - Thread safety: entry points may be called from several host threads; the error text
  *     is per thread.
@@ -49,7 +58,10 @@
 extern "C" {
 #endif
 
-#define NVFP4KV_ABI_VERSION 3
+#define NVFP4KV_ABI_VERSION 4
+
+/* Bytes of the optional `workspace` of the bulk-copy kernels (see the conventions). */
+#define NVFP4_WORKSPACE_BYTES 16
 
 /* Return codes. */
 typedef int32_t nvfp4_status;
@@ -187,7 +199,7 @@ nvfp4_status nvfp4_quantize_append_paged(
     nvfp4_paged_cache v_cache, int32_t page_size, int32_t kv_layout,
     const int32_t* kv_indices, int64_t num_kv_indices, const int32_t* kv_indptr,
     const int32_t* kv_last_page_len, int32_t batch_size, float k_scale, float v_scale,
-    const nvfp4_4over6_config* recipe, int32_t* dev_status, void* stream);
+    const nvfp4_4over6_config* recipe, int32_t* dev_status, void* workspace, void* stream);
 
 /* nvfp4_quantize_append_paged with the two global decode scales read from device memory
  * (k_scale, v_scale: one float each, for example the outputs of nvfp4_make_global_scale),
@@ -202,7 +214,7 @@ nvfp4_status nvfp4_quantize_append_paged_dev_scale(
     const int32_t* kv_indices, int64_t num_kv_indices, const int32_t* kv_indptr,
     const int32_t* kv_last_page_len, int32_t batch_size, const float* k_scale,
     const float* v_scale, const nvfp4_4over6_config* recipe, int32_t* dev_status,
-    void* stream);
+    void* workspace, void* stream);
 
 /* Dequantize a paged NVFP4 cache into contiguous outputs
  * ("flashinfer.quantization.nvfp4_kv_dequantize_paged").
@@ -224,7 +236,7 @@ nvfp4_status nvfp4_dequantize_paged(
     int32_t table_dtype, int32_t max_pages_per_request, const int32_t* seq_lens,
     int32_t batch_size, const float* k_scale, const float* v_scale, void* output_k,
     void* output_v, int32_t out_dtype, int32_t max_seq_len, int32_t* dev_status,
-    void* stream);
+    void* workspace, void* stream);
 
 /* Shape of the FP8 copy ("nvfp4_kv_materialize_fp8", returns): max_pages_per_seq =
  * ceil(max_kv_len / page_size); the copy has num_pages + 1 pages, where num_pages is the
@@ -267,7 +279,8 @@ nvfp4_status nvfp4_materialize_fp8(
     int32_t max_num_pages, int32_t uses_shared_paged_kv_idx, const int32_t* seq_lens,
     int32_t batch_size, int32_t max_kv_len, const int32_t* kv_page_indptr, int64_t num_pages,
     uint8_t* out, int64_t out_num_pages, int32_t* fp8_block_tables,
-    int32_t zero_fp8_block_tables, int32_t v_scale_layout, int32_t* dev_status, void* stream);
+    int32_t zero_fp8_block_tables, int32_t v_scale_layout, int32_t* dev_status,
+    void* workspace, void* stream);
 
 /* A materialize launch prepared once ("flashinfer.quantization" index, NVFP4KVMaterializer:
  * the static layout is checked when the materializer is built, so that each run() costs
@@ -319,7 +332,7 @@ nvfp4_status nvfp4_materializer_run(const nvfp4_materializer* m, nvfp4_paged_cac
                                     const int32_t* kv_page_indptr, int64_t num_pages,
                                     uint8_t* out, int64_t out_num_pages,
                                     int32_t* fp8_block_tables, int32_t* dev_status,
-                                    void* stream);
+                                    void* workspace, void* stream);
 
 /* Quantize a contiguous fp16/bf16 tensor to NVFP4 with linear block scales
  * ("flashinfer.quantization" index, "FP4 KV Cache Quantization": nvfp4_kv_quantize).
@@ -338,7 +351,8 @@ nvfp4_status nvfp4_materializer_run(const nvfp4_materializer* m, nvfp4_paged_cac
 nvfp4_status nvfp4_kv_quantize(const void* input, int32_t dtype, int64_t rows, int32_t cols,
                                int64_t row_stride, const float* global_scale,
                                const nvfp4_4over6_config* recipe, uint8_t* fp4_out,
-                               uint8_t* sf_out, int32_t* dev_status, void* stream);
+                               uint8_t* sf_out, int32_t* dev_status, void* workspace,
+                               void* stream);
 
 /* Dequantize a contiguous NVFP4 tensor with linear block scales
  * ("flashinfer.quantization" index, "FP4 KV Cache Quantization": nvfp4_kv_dequantize):

@@ -109,32 +109,32 @@ def load() -> ctypes.CDLL:
         L.nvfp4_quantize_append_paged.restype = i32
         L.nvfp4_quantize_append_paged.argtypes = [
             vp, vp, i32, i64, i32, i32, i64, i64, vp, vp, _Cache, _Cache, i32, i32, vp, i64, vp,
-            vp, i32, f32, f32, vp, vp, vp]
+            vp, i32, f32, f32, vp, vp, vp, vp]
         L.nvfp4_quantize_append_paged_dev_scale.restype = i32
         L.nvfp4_quantize_append_paged_dev_scale.argtypes = [
             vp, vp, i32, i64, i32, i32, i64, i64, vp, vp, _Cache, _Cache, i32, i32, vp, i64, vp,
-            vp, i32, vp, vp, vp, vp, vp]
+            vp, i32, vp, vp, vp, vp, vp, vp]
         L.nvfp4_dequantize_paged.restype = i32
         L.nvfp4_dequantize_paged.argtypes = [
             _Cache, _Cache, i32, i32, i32, i32, vp, i32, i32, vp, i32, vp, vp, vp, vp, i32, i32,
-            vp, vp]
+            vp, vp, vp]
         L.nvfp4_materialize_fp8_out_pages.restype = i32
         L.nvfp4_materialize_fp8_out_pages.argtypes = [i32, i32, i32, i64, vp, vp]
         L.nvfp4_materialize_fp8.restype = i32
         L.nvfp4_materialize_fp8.argtypes = [
             _Cache, _Cache, i32, i32, i32, i32, vp, i32, i32, vp, i32, i32, vp, i64, vp, i64, vp,
-            i32, i32, vp, vp]
+            i32, i32, vp, vp, vp]
         L.nvfp4_materializer_prepare.restype = i32
         L.nvfp4_materializer_prepare.argtypes = [vp, i32, i32, i32, i32, i32, i32, i64, i64, i32]
         L.nvfp4_materializer_run.restype = i32
         L.nvfp4_materializer_run.argtypes = [
-            vp, _Cache, _Cache, vp, i32, vp, i32, i32, vp, i64, vp, i64, vp, vp, vp]
+            vp, _Cache, _Cache, vp, i32, vp, i32, i32, vp, i64, vp, i64, vp, vp, vp, vp]
         L.nvfp4_4over6_code.restype = i32
         L.nvfp4_4over6_code.argtypes = [vp, vp]
         L.nvfp4_4over6_from_code.restype = i32
         L.nvfp4_4over6_from_code.argtypes = [i64, vp, vp]
         L.nvfp4_kv_quantize.restype = i32
-        L.nvfp4_kv_quantize.argtypes = [vp, i32, i64, i32, i64, vp, vp, vp, vp, vp, vp]
+        L.nvfp4_kv_quantize.argtypes = [vp, i32, i64, i32, i64, vp, vp, vp, vp, vp, vp, vp]
         L.nvfp4_kv_dequantize.restype = i32
         L.nvfp4_kv_dequantize.argtypes = [vp, vp, i64, i32, vp, vp, i32, vp, vp]
         _lib = L
@@ -157,6 +157,34 @@ def _ptr(t: Optional[torch.Tensor]):
 
 def _stream(device: torch.device):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+# Work-distribution workspaces (NVFP4_WORKSPACE_BYTES of device memory, zero on first use
+# and left zero by every kernel), one per (device, stream): calls on one stream run one at
+# a time, so they can share one; calls on different streams may overlap and get their own.
+_workspaces = {}
+_dynamic_schedule = True
+
+
+def set_dynamic_schedule(enabled: bool) -> None:
+    """Whether the bulk-copy kernels take work items from a shared counter (the default)
+    or give each CTA a fixed share. The results are the same either way."""
+    global _dynamic_schedule
+    _dynamic_schedule = bool(enabled)
+
+
+def _ws_stream(device: torch.device):
+    """(workspace, stream) arguments for a call on the current stream of `device`."""
+    stream = torch.cuda.current_stream(device)
+    handle = stream.cuda_stream
+    ws = None
+    if _dynamic_schedule:
+        key = (device.index, handle)
+        ws = _workspaces.get(key)
+        if ws is None and not torch.cuda.is_current_stream_capturing():
+            ws = torch.zeros(2, dtype=torch.int64, device=device)  # 16 bytes, on this stream
+            _workspaces[key] = ws
+    return (None if ws is None else ctypes.c_void_p(ws.data_ptr())), ctypes.c_void_p(handle)
 
 
 def _layout(kv_layout: Union[str, int]) -> int:
@@ -281,7 +309,7 @@ def nvfp4_quantize_append_paged(append_key: torch.Tensor, append_value: torch.Te
               append_key.stride(0) if nnz else H * D, append_value.stride(0) if nnz else H * D,
               _ptr(batch_indices), _ptr(positions), kc._c(), vc._c(), ps, layout,
               _ptr(kv_indices), kv_indices.numel(), _ptr(kv_indptr), _ptr(kv_last_page_len), B)
-    tail = (_recipe(nvfp4_4over6), _ptr(dev_status), _stream(append_key.device))
+    tail = (_recipe(nvfp4_4over6), _ptr(dev_status), *_ws_stream(append_key.device))
     if isinstance(k_scale, torch.Tensor) or isinstance(v_scale, torch.Tensor):
         # scales held on the device (e.g. from nvfp4_make_global_scale): no host round trip
         for t in (k_scale, v_scale):
@@ -323,7 +351,7 @@ def nvfp4_dequantize_paged(paged_kv_cache, kv_cache_sf, block_tables: torch.Tens
         kc._c(), vc._c(), ps, H, D, layout, _ptr(block_tables),
         I64 if block_tables.dtype == torch.int64 else I32, block_tables.shape[1],
         _ptr(seq_lens), B, _ptr(k_scale), _ptr(v_scale), _ptr(output_k), _ptr(output_v),
-        _dtype_code(output_k.dtype), L, _ptr(dev_status), _stream(output_k.device)))
+        _dtype_code(output_k.dtype), L, _ptr(dev_status), *_ws_stream(output_k.device)))
 
 
 def nvfp4_materialize_fp8_out_pages(batch_size: int, max_kv_len: int, page_size: int,
@@ -380,7 +408,7 @@ def nvfp4_materialize_fp8(k_cache: torch.Tensor, v_cache: torch.Tensor,
         int(shared), _ptr(seq_lens), B, int(max_kv_len), _ptr(kv_page_indptr),
         -1 if num_pages is None else int(num_pages), _ptr(out), out.shape[0],
         _ptr(fp8_block_tables), int(bool(zero_fp8_block_tables)),
-        _sf_layout(v_block_scales_layout), _ptr(dev_status), _stream(dev)))
+        _sf_layout(v_block_scales_layout), _ptr(dev_status), *_ws_stream(dev)))
     return out, fp8_block_tables
 
 
@@ -445,7 +473,7 @@ class NVFP4KVMaterializer:
         _check("nvfp4_materializer_run", self._lib.nvfp4_materializer_run(
             ctypes.byref(m), kc._c(), vc._c(), _ptr(block_tables), block_tables.shape[-1],
             _ptr(seq_lens), B, mpps, _ptr(kv_page_indptr), out.shape[0] - 1, _ptr(out),
-            out.shape[0], _ptr(fp8_block_tables), _ptr(dev_status), _stream(self.device)))
+            out.shape[0], _ptr(fp8_block_tables), _ptr(dev_status), *_ws_stream(self.device)))
         return out, fp8_block_tables
 
 
@@ -484,7 +512,7 @@ def nvfp4_kv_quantize(input: torch.Tensor, global_scale,
     _check("nvfp4_kv_quantize", load().nvfp4_kv_quantize(
         _ptr(x2), _dtype_code(input.dtype), rows, cols, x2.stride(0) if rows > 1 else cols,
         _ptr(gs), _recipe(nvfp4_4over6), _ptr(fp4), _ptr(sf), _ptr(dev_status),
-        _stream(input.device)))
+        *_ws_stream(input.device)))
     return fp4, sf
 
 

@@ -98,6 +98,12 @@ namespace {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+nvfp4_status check_workspace(const char* fn, const void* workspace) {
+  if (workspace && !aligned(workspace, 8))
+    return fail(NVFP4_ERR_ALIGNMENT, std::string(fn) + ": workspace must be 8-byte aligned");
+  return NVFP4_OK;
+}
+
 nvfp4_status check_recipe(const nvfp4_4over6_config* r) {
   if (!r) return NVFP4_OK;
   if (!(std::isfinite(r->e4m3_max) && r->e4m3_max > 0.0f && r->e4m3_max <= 448.0f))
@@ -182,9 +188,10 @@ nvfp4_status append_impl(
     const int32_t* kv_indices, int64_t num_kv_indices, const int32_t* kv_indptr,
     const int32_t* kv_last_page_len, int32_t batch_size, float k_scale, float v_scale,
     const float* k_dev, const float* v_dev, const nvfp4_4over6_config* recipe,
-    int32_t* dev_status, void* stream) {
+    int32_t* dev_status, void* workspace, void* stream) {
   clear_error();
   if (nvfp4_status st = check_recipe(recipe)) return st;
+  if (nvfp4_status st = check_workspace(fn, workspace)) return st;
   if (nvfp4_status st = check_geometry(fn, page_size, num_kv_heads, head_dim, kv_layout)) return st;
   if (dtype != NVFP4_F16 && dtype != NVFP4_BF16)
     return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_quantize_append_paged: dtype must be NVFP4_F16 or NVFP4_BF16");
@@ -242,6 +249,7 @@ nvfp4_status append_impl(
   a.neg_zero = 0x80000000u;
   a.pipe = pipe_test_from_env();
   a.status = dev_status;
+  a.workspace = workspace;
   int mode = 0;
   if (recipe) mode = 1 + (recipe->err_mode == NVFP4_ERR_MSE ? 1 : 0) + (recipe->err_use_fast_math ? 2 : 0);
   const bool vec256 = aligned(append_key, 32) && aligned(append_value, 32) &&
@@ -260,12 +268,12 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_append_paged(
     nvfp4_paged_cache v_cache, int32_t page_size, int32_t kv_layout,
     const int32_t* kv_indices, int64_t num_kv_indices, const int32_t* kv_indptr,
     const int32_t* kv_last_page_len, int32_t batch_size, float k_scale, float v_scale,
-    const nvfp4_4over6_config* recipe, int32_t* dev_status, void* stream) {
+    const nvfp4_4over6_config* recipe, int32_t* dev_status, void* workspace, void* stream) {
   return append_impl("nvfp4_quantize_append_paged", append_key, append_value, dtype, nnz,
                      num_kv_heads, head_dim, key_row_stride, value_row_stride, batch_indices,
                      positions, k_cache, v_cache, page_size, kv_layout, kv_indices,
                      num_kv_indices, kv_indptr, kv_last_page_len, batch_size, k_scale, v_scale,
-                     nullptr, nullptr, recipe, dev_status, stream);
+                     nullptr, nullptr, recipe, dev_status, workspace, stream);
 }
 
 NVFP4_EXPORT nvfp4_status nvfp4_quantize_append_paged_dev_scale(
@@ -276,14 +284,14 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_append_paged_dev_scale(
     const int32_t* kv_indices, int64_t num_kv_indices, const int32_t* kv_indptr,
     const int32_t* kv_last_page_len, int32_t batch_size, const float* k_scale,
     const float* v_scale, const nvfp4_4over6_config* recipe, int32_t* dev_status,
-    void* stream) {
+    void* workspace, void* stream) {
   if (k_scale == nullptr || v_scale == nullptr)
     return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_quantize_append_paged_dev_scale: null scale pointer");
   return append_impl("nvfp4_quantize_append_paged_dev_scale", append_key, append_value, dtype,
                      nnz, num_kv_heads, head_dim, key_row_stride, value_row_stride,
                      batch_indices, positions, k_cache, v_cache, page_size, kv_layout,
                      kv_indices, num_kv_indices, kv_indptr, kv_last_page_len, batch_size, 1.0f,
-                     1.0f, k_scale, v_scale, recipe, dev_status, stream);
+                     1.0f, k_scale, v_scale, recipe, dev_status, workspace, stream);
 }
 
 NVFP4_EXPORT nvfp4_status nvfp4_4over6_code(const nvfp4_4over6_config* recipe, int64_t* code) {
@@ -331,10 +339,12 @@ NVFP4_EXPORT nvfp4_status nvfp4_kv_quantize(const void* input, int32_t dtype, in
                                             const float* global_scale,
                                             const nvfp4_4over6_config* recipe,
                                             uint8_t* fp4_out, uint8_t* sf_out,
-                                            int32_t* dev_status, void* stream) {
+                                            int32_t* dev_status, void* workspace,
+                                            void* stream) {
   clear_error();
   const char* fn = "nvfp4_kv_quantize";
   if (nvfp4_status st = check_recipe(recipe)) return st;
+  if (nvfp4_status st = check_workspace(fn, workspace)) return st;
   if (dtype != NVFP4_F16 && dtype != NVFP4_BF16)
     return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_kv_quantize: dtype must be NVFP4_F16 or NVFP4_BF16");
   if (cols <= 0 || cols % 16 != 0)
@@ -368,6 +378,7 @@ NVFP4_EXPORT nvfp4_status nvfp4_kv_quantize(const void* input, int32_t dtype, in
   a.neg_zero = 0x80000000u;
   a.pipe = pipe_test_from_env();
   a.status = dev_status;
+  a.workspace = workspace;
   a.contig = 1;
   int mode = 0;
   if (recipe) mode = 1 + (recipe->err_mode == NVFP4_ERR_MSE ? 1 : 0) + (recipe->err_use_fast_math ? 2 : 0);
@@ -408,9 +419,10 @@ NVFP4_EXPORT nvfp4_status nvfp4_dequantize_paged(
     int32_t table_dtype, int32_t max_pages_per_request, const int32_t* seq_lens,
     int32_t batch_size, const float* k_scale, const float* v_scale, void* output_k,
     void* output_v, int32_t out_dtype, int32_t max_seq_len, int32_t* dev_status,
-    void* stream) {
+    void* workspace, void* stream) {
   clear_error();
   const char* fn = "nvfp4_dequantize_paged";
+  if (nvfp4_status st = check_workspace(fn, workspace)) return st;
   if (nvfp4_status st = check_geometry(fn, page_size, num_kv_heads, head_dim, kv_layout)) return st;
   if (out_dtype != NVFP4_F16 && out_dtype != NVFP4_BF16)
     return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_dequantize_paged: out_dtype must be NVFP4_F16 or NVFP4_BF16");
@@ -449,6 +461,7 @@ NVFP4_EXPORT nvfp4_status nvfp4_dequantize_paged(
   a.L = max_seq_len;
   a.pipe = pipe_test_from_env();
   a.status = dev_status;
+  a.workspace = workspace;
   const bool vec256 = aligned(output_k, 32) && aligned(output_v, 32);
   return launch_dequant(a, out_dtype == NVFP4_BF16, table_dtype == NVFP4_I64, vec256,
                         static_cast<cudaStream_t>(stream));
@@ -474,9 +487,11 @@ NVFP4_EXPORT nvfp4_status nvfp4_materialize_fp8(
     int32_t max_num_pages, int32_t uses_shared_paged_kv_idx, const int32_t* seq_lens,
     int32_t batch_size, int32_t max_kv_len, const int32_t* kv_page_indptr, int64_t num_pages,
     uint8_t* out, int64_t out_num_pages, int32_t* fp8_block_tables,
-    int32_t zero_fp8_block_tables, int32_t v_scale_layout, int32_t* dev_status, void* stream) {
+    int32_t zero_fp8_block_tables, int32_t v_scale_layout, int32_t* dev_status,
+    void* workspace, void* stream) {
   clear_error();
   const char* fn = "nvfp4_materialize_fp8";
+  if (nvfp4_status st = check_workspace(fn, workspace)) return st;
   if (v_scale_layout != NVFP4_SF_LINEAR && v_scale_layout != NVFP4_SF_INTERLEAVED4)
     return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materialize_fp8: v_scale_layout must be NVFP4_SF_LINEAR or NVFP4_SF_INTERLEAVED4");
   if (nvfp4_status st = check_geometry(fn, page_size, num_kv_heads, head_dim, kv_layout)) return st;
@@ -533,6 +548,7 @@ NVFP4_EXPORT nvfp4_status nvfp4_materialize_fp8(
   a.v_interleaved = v_scale_layout == NVFP4_SF_INTERLEAVED4 ? 1 : 0;
   a.pipe = pipe_test_from_env();
   a.status = dev_status;
+  a.workspace = workspace;
   if (batch_size == 0) {
     // nothing active: the copy is just its zero page
     const size_t bytes = static_cast<size_t>(2) * num_kv_heads * page_size * head_dim;
@@ -605,8 +621,9 @@ NVFP4_EXPORT nvfp4_status nvfp4_materializer_run(
     const int32_t* block_tables, int32_t max_num_pages, const int32_t* seq_lens,
     int32_t batch_size, int32_t max_pages_per_seq, const int32_t* kv_page_indptr,
     int64_t num_pages, uint8_t* out, int64_t out_num_pages, int32_t* fp8_block_tables,
-    int32_t* dev_status, void* stream) {
+    int32_t* dev_status, void* workspace, void* stream) {
   clear_error();
+  if (nvfp4_status st = check_workspace("nvfp4_materializer_run", workspace)) return st;
   if (!m || m->magic != kMaterializerMagic)
     return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_materializer_run: m was not prepared");
   int dev = -1;
@@ -665,6 +682,7 @@ NVFP4_EXPORT nvfp4_status nvfp4_materializer_run(
   a.v_interleaved = m->v_scale_layout == NVFP4_SF_INTERLEAVED4 ? 1 : 0;
   a.pipe = m->stall_test ? PipeTest{1u << 12, 1, 0} : PipeTest{kWaitLimit, 0, 0};
   a.status = dev_status;
+  a.workspace = workspace;
   const MaterializeLaunch c{m->bulk, m->max_batch_size, m->smem_bytes, m->grid};
   return launch_materialize_prepared(a, c, static_cast<cudaStream_t>(stream));
 }

@@ -490,7 +490,8 @@ inline AppendTmaLayout append_tma_layout(uint32_t rows, uint32_t row_bytes, uint
   L.stages_off = round_up(sizeof(Tables), 128);
   L.bars_off = L.stages_off + static_cast<uint32_t>(ns) * L.stage_bytes;
   L.misc_off = L.bars_off + 2u * static_cast<uint32_t>(ns) * 8u;
-  L.total = L.misc_off + 4u * (1u + static_cast<uint32_t>(ns));
+  // misc: abort flag, per-stage issue counts, per-stage tile index
+  L.total = L.misc_off + 4u * (1u + 2u * static_cast<uint32_t>(ns));
   return L;
 }
 
@@ -504,6 +505,9 @@ __host__ __device__ constexpr int append_threads(int mode) {
   return 32 * append_consumer_warps(mode) + 32;
 }
 constexpr int kAppendCtasPerSm = 2;
+// Tiles a producer takes from the work queue per atomic: two consecutive tiles (measured
+// faster than one or a fixed share; consecutive rows land in the same pages).
+constexpr int kTilesPerFetch = 2;
 
 // NKV: tensors per stage, 2 (K and V, paged) or 1 (the contiguous form). FIXED: a row's
 // blocks divide the consumer threads (chosen at launch), so each thread keeps one (head, block).
@@ -521,9 +525,13 @@ __global__ void __launch_bounds__(append_threads(MODE), kAppendCtasPerSm)
   volatile int32_t* s_abort = reinterpret_cast<int32_t*>(smem + L.misc_off);
   volatile uint32_t* s_issued = reinterpret_cast<uint32_t*>(smem + L.misc_off + 4);
   const int ns = L.ns;
+  // tile of each stage (-1: no more tiles)
+  volatile int32_t* s_tile = reinterpret_cast<int32_t*>(smem + L.misc_off + 4 + 4 * ns);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float gs[2];
-  if (!load_scales(a, gs)) return;  // uniform over the CTA, before any barrier or copy
+  // uniform over the grid, before any barrier, copy or work taken from the queue
+  if (!load_scales(a, gs)) return;
+  const WorkQueue q = work_queue(a.workspace);
   if (threadIdx.x == 0) {
     for (int s = 0; s < ns; ++s) {
       mbar_init(full + s, 1);
@@ -542,11 +550,17 @@ __global__ void __launch_bounds__(append_threads(MODE), kAppendCtasPerSm)
   if (warp == kConsumerWarps) {
     int s = 0;
     uint32_t phase = 0, round = 0;  // phase = parity of `round`, the stage's fill count
-    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    ItemCursor cur;
+    if (lane == 0) cur.init(q, kTilesPerFetch);
+    for (;;) {
+      long long tile = 0;
+      if (lane == 0) tile = cur.next(q, tiles);
+      tile = __shfl_sync(0xFFFFFFFFu, tile, 0);
+      const bool end = tile >= tiles;
       // (test control: withhold the first stage so that the consumers' wait expires)
-      const bool withhold = a.pipe.stall && round == 0 && s == 0;
-      const int64_t row0 = tile * L.rows;
-      const uint32_t nrows = withhold ? 0u
+      const bool withhold = !end && a.pipe.stall && round == 0 && s == 0;
+      const int64_t row0 = end ? 0 : tile * L.rows;
+      const uint32_t nrows = (end || withhold) ? 0u
           : static_cast<uint32_t>(min(static_cast<int64_t>(L.rows), a.nnz - row0));
       // Resolve this tile's destinations (a chain of dependent index loads, one row per
       // lane: at most 32 rows) while the consumers still work on the stage it will use.
@@ -562,9 +576,19 @@ __global__ void __launch_bounds__(append_threads(MODE), kAppendCtasPerSm)
         }
         break;
       }
+      if (end) {
+        if (lane == 0) {
+          s_tile[s] = -1;
+          mbar_arrive(full + s);
+          s_issued[s] = round + 1;
+        }
+        __syncwarp();
+        break;
+      }
       uint8_t* st = stages + static_cast<uint32_t>(s) * L.stage_bytes;
       RowDst* dst = reinterpret_cast<RowDst*>(st + nkv * tile_bytes);
       if (static_cast<uint32_t>(lane) < nrows) dst[lane] = d;
+      if (lane == 0) s_tile[s] = static_cast<int32_t>(tile);
       __syncwarp();
       if (lane == 0 && !withhold) mbar_arrive_expect_tx(full + s, nkv * nrows * L.row_bytes);
       __syncwarp();
@@ -610,7 +634,7 @@ __global__ void __launch_bounds__(append_threads(MODE), kAppendCtasPerSm)
     constexpr bool kExact = decltype(exact_tag)::value;
     int s = 0;
     uint32_t phase = 0;
-    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    for (;;) {
       if (*s_abort || !mbar_wait(full + s, phase, a.pipe.wait_limit)) {
         if (lane == 0) {
           *s_abort = 1;
@@ -618,6 +642,8 @@ __global__ void __launch_bounds__(append_threads(MODE), kAppendCtasPerSm)
         }
         break;
       }
+      const int64_t tile = s_tile[s];
+      if (tile < 0) break;
       const uint8_t* st = stages + static_cast<uint32_t>(s) * L.stage_bytes;
       const RowDst* dst = reinterpret_cast<const RowDst*>(st + nkv * tile_bytes);
       const int32_t nrows =
@@ -662,6 +688,7 @@ __global__ void __launch_bounds__(append_threads(MODE), kAppendCtasPerSm)
   if (threadIdx.x == 0) {
     for (int s = 0; s < ns; ++s)
       if (s_issued[s] > 0) mbar_wait(full + s, (s_issued[s] - 1) & 1u, a.pipe.wait_limit);
+    finish_queue(q);
   }
 }
 
@@ -696,6 +723,7 @@ nvfp4_status launch_tma(const AppendArgs& a, uint32_t row_bytes, uint32_t nkv,
                                            "nvfp4_quantize_append_paged");
   if (st != NVFP4_OK) return st;
   const int64_t tiles = (a.nnz + rows - 1) / rows;
+  if (tiles > INT32_MAX) return fail(NVFP4_ERR_UNSUPPORTED, "nvfp4_quantize_append_paged: more than 2^31 tiles");
   const int64_t cap = static_cast<int64_t>(sm_count()) *
                       blocks_per_sm(reinterpret_cast<const void*>(kern), append_threads(MODE),
                                     L.total);

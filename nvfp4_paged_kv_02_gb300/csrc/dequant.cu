@@ -24,6 +24,9 @@ namespace {
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kTmaThreads = kConsumers + 32;
+// Items a producer takes from the work queue per atomic (a page of K or V is one item;
+// one at a time measured best: the output of one item is already a long contiguous run).
+constexpr int kItemsPerFetch = 1;
 
 // 128-thread CTAs (about a dozen resident per SM) each load a whole 16-token page's blocks
 // per thread before decoding, so many pages' loads are in flight at once.
@@ -171,12 +174,38 @@ __global__ void __launch_bounds__(kTmaThreads, 4) dequant_tma_kernel(const Dequa
   });
   const int64_t items = 2 * static_cast<int64_t>(s_cum[a.B - 1]);
 
+  const WorkQueue q = work_queue(a.workspace);
   if (warp == kConsumerWarps) {
-    // producer: lane 0 issues, the warp stays converged
+    // producer: lane 0 takes the items and issues, the warp stays converged
     int s = 0;
     uint32_t round = 0;  // how many times stage s has been used before
-    for (int64_t item = blockIdx.x; item < items;
-         item += gridDim.x, s = (s + 1 == ns) ? 0 : s + 1, round += (s == 0)) {
+    ItemCursor cur;
+    if (lane == 0) cur.init(q, kItemsPerFetch);
+    for (;; s = (s + 1 == ns) ? 0 : s + 1, round += (s == 0)) {
+      // the next item and its source page, resolved while the consumers still work on the
+      // stage it will use
+      long long item = 0;
+      if (lane == 0) item = cur.next(q, items);
+      item = __shfl_sync(0xFFFFFFFFu, item, 0);
+      const bool end = item >= items;
+      StageMeta m{0, 0, 0, kStageEnd};
+      int64_t page = 0;
+      if (lane == 0 && !end) {
+        const int kv = static_cast<int>(item & 1);
+        const int32_t pi = static_cast<int32_t>(item >> 1);
+        const int32_t b = scan_find(s_cum, a.B, pi);
+        const int32_t j = pi - (b > 0 ? s_cum[b - 1] : 0);
+        const int32_t len = min(__ldg(a.seq_lens + b), cap);
+        const int32_t t0 = j * ps;
+        const int64_t tcol = static_cast<int64_t>(b) * a.max_pages + j;
+        page = BT64 ? __ldg(reinterpret_cast<const int64_t*>(a.block_tables) + tcol)
+                    : __ldg(reinterpret_cast<const int32_t*>(a.block_tables) + tcol);
+        const bool valid = page >= 0 && page < (kv ? a.vc.num_pages : a.kc.num_pages);
+        m.f0 = b;
+        m.f1 = t0;
+        m.f2 = min(ps, len - t0);
+        m.flags = kv | (valid ? 2 : 0);
+      }
       bool ok = true;
       if (lane == 0) ok = mbar_wait(empty + s, (round & 1u) ^ 1u, a.pipe.wait_limit) && !*s_abort;
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -188,40 +217,26 @@ __global__ void __launch_bounds__(kTmaThreads, 4) dequant_tma_kernel(const Dequa
         break;
       }
       // (test control: withhold the first stage so that the consumers' wait expires)
-      if (lane == 0 && !(a.pipe.stall && round == 0 && s == 0)) {
-        const int kv = static_cast<int>(item & 1);
-        const int32_t pi = static_cast<int32_t>(item >> 1);
-        const int32_t b = scan_find(s_cum, a.B, pi);
-        const int32_t j = pi - (b > 0 ? s_cum[b - 1] : 0);
-        const int32_t len = min(__ldg(a.seq_lens + b), cap);
-        const int32_t t0 = j * ps;
-        const int64_t tcol = static_cast<int64_t>(b) * a.max_pages + j;
-        const int64_t page =
-            BT64 ? __ldg(reinterpret_cast<const int64_t*>(a.block_tables) + tcol)
-                 : __ldg(reinterpret_cast<const int32_t*>(a.block_tables) + tcol);
-        const uint8_t* data = kv ? a.vc.data : a.kc.data;
-        const uint8_t* sf = kv ? a.vc.sf : a.kc.sf;
-        const int64_t dps = kv ? a.vc.data_page_stride : a.kc.data_page_stride;
-        const int64_t sps = kv ? a.vc.sf_page_stride : a.kc.sf_page_stride;
-        const bool valid = page >= 0 && page < (kv ? a.vc.num_pages : a.kc.num_pages);
-        StageMeta m;
-        m.f0 = b;
-        m.f1 = t0;
-        m.f2 = min(ps, len - t0);
-        m.flags = kv | (valid ? 2 : 0);
+      if (lane == 0 && (end || !(a.pipe.stall && round == 0 && s == 0))) {
         meta[s] = m;
         uint8_t* st = stages + static_cast<uint32_t>(s) * L.stage_bytes;
-        if (valid) {
+        if (m.flags & 2) {
+          const int kv = m.flags & 1;
+          const uint8_t* data = kv ? a.vc.data : a.kc.data;
+          const uint8_t* sf = kv ? a.vc.sf : a.kc.sf;
+          const int64_t dps = kv ? a.vc.data_page_stride : a.kc.data_page_stride;
+          const int64_t sps = kv ? a.vc.sf_page_stride : a.kc.sf_page_stride;
           mbar_arrive_expect_tx(full + s, L.codes_bytes + L.sf_bytes);
           bulk_g2s(st, data + page * dps, L.codes_bytes, full + s);
           bulk_g2s(st + L.sf_off, sf + page * sps, L.sf_bytes, full + s);
         } else {
-          flag(a.status, NVFP4_DEV_BAD_PAGE);
+          if (!end) flag(a.status, NVFP4_DEV_BAD_PAGE);
           mbar_arrive(full + s);
         }
         s_issued[s] = round + 1;
       }
       __syncwarp();
+      if (end) break;
     }
   } else {
     const int ct = threadIdx.x;  // 0 .. kConsumers-1
@@ -231,8 +246,7 @@ __global__ void __launch_bounds__(kTmaThreads, 4) dequant_tma_kernel(const Dequa
     const float gs_v = __ldg(a.v_scale);
     int s = 0;
     uint32_t round = 0;  // how many times stage s has been used before
-    for (int64_t item = blockIdx.x; item < items;
-         item += gridDim.x, s = (s + 1 == ns) ? 0 : s + 1, round += (s == 0)) {
+    for (;; s = (s + 1 == ns) ? 0 : s + 1, round += (s == 0)) {
       if (*s_abort || !mbar_wait(full + s, round & 1u, a.pipe.wait_limit)) {
         if (lane == 0) {
           *s_abort = 1;
@@ -241,6 +255,7 @@ __global__ void __launch_bounds__(kTmaThreads, 4) dequant_tma_kernel(const Dequa
         break;
       }
       const StageMeta m = meta[s];
+      if (m.flags & kStageEnd) break;
       if (m.flags & 2) {
         const uint8_t* st = stages + static_cast<uint32_t>(s) * L.stage_bytes;
         const uint8_t* sfp = st + L.sf_off;
@@ -282,6 +297,7 @@ __global__ void __launch_bounds__(kTmaThreads, 4) dequant_tma_kernel(const Dequa
   if (threadIdx.x == 0) {
     for (int s = 0; s < ns; ++s)
       if (s_issued[s] > 0) mbar_wait(full + s, (s_issued[s] - 1) & 1u, a.pipe.wait_limit);
+    finish_queue(q);
   }
 }
 

@@ -61,6 +61,7 @@ struct AppendArgs {
   uint32_t neg_zero;  // 0x80000000 (-0.0f), passed at run time for hsq2_rn
   PipeTest pipe;
   int32_t* status;
+  void* workspace;  // NVFP4_WORKSPACE_BYTES (dynamic schedule of the ring kernel) or null
   // Contiguous form (nvfp4_kv_quantize): row i goes to kc.data + i * H*D/2 and
   // kc.sf + i * H*D/16; no index arrays are read, and v is null.
   int32_t contig;
@@ -85,6 +86,7 @@ struct DequantArgs {
   int32_t L;
   PipeTest pipe;
   int32_t* status;
+  void* workspace;  // NVFP4_WORKSPACE_BYTES (dynamic schedule of the ring kernel) or null
 };
 // Contiguous dequantize (nvfp4_kv_dequantize): block k of the flattened [rows, cols] codes
 // (8 bytes at codes + 8k, scale byte sf[k]) becomes 16 outputs at out + 32k bytes.
@@ -120,6 +122,7 @@ struct MaterializeArgs {
   int32_t v_interleaved;  // V scales in the 4-token-interleaved layout (HND pages)
   PipeTest pipe;
   int32_t* status;
+  void* workspace;  // NVFP4_WORKSPACE_BYTES (dynamic schedule of the ring kernel) or null
 };
 nvfp4_status launch_materialize(const MaterializeArgs& a, cudaStream_t stream);
 

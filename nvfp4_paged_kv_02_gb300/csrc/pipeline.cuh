@@ -82,6 +82,72 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// ---- work distribution among the persistent CTAs ----------------------------------------
+//
+// Without a workspace each CTA's producer takes the items blockIdx.x, blockIdx.x + gridDim.x,
+// ... (a fixed share). With one (NVFP4_WORKSPACE_BYTES of device memory, zero when the
+// launch starts), the producers take the next item from a counter there as their stages
+// free up, so CTAs on SMs that run ahead take more items and the last wave ends together.
+// The last CTA to finish sets the workspace back to zero for the next launch on its stream.
+struct WorkQueue {
+  unsigned long long* next;  // item counter (null: fixed shares)
+  unsigned int* done;        // CTAs that have finished taking items
+};
+
+__host__ __device__ inline WorkQueue work_queue(void* workspace) {
+  WorkQueue q;
+  q.next = static_cast<unsigned long long*>(workspace);
+  q.done = workspace ? reinterpret_cast<unsigned int*>(static_cast<unsigned char*>(workspace) + 8)
+                     : nullptr;
+  return q;
+}
+
+// The items of one CTA's producer (one thread calls it). From the queue they come `per`
+// at a time, consecutive (one atomic per batch: a single counter takes a few hundred
+// million atomics a second, which small items would otherwise reach, and consecutive items
+// of one CTA write neighbouring output); in fixed shares one at a time. The next batch is
+// requested when the current one is started, so the atomic's latency overlaps the work on
+// the current items.
+struct ItemCursor {
+  long long mine, base, next_base;
+  int i, per;
+
+  __device__ __forceinline__ long long take(const WorkQueue& q) {
+    if (q.next) return static_cast<long long>(atomicAdd(q.next, static_cast<unsigned long long>(per)));
+    const long long it = mine;
+    mine += gridDim.x;
+    return it;
+  }
+  __device__ __forceinline__ void init(const WorkQueue& q, int items_per_fetch) {
+    mine = blockIdx.x;
+    i = 0;
+    per = q.next ? (items_per_fetch > 0 ? items_per_fetch : 1) : 1;
+    next_base = 0;
+    base = take(q);
+  }
+  // The next item; one at or past `limit` means there is no more work.
+  __device__ __forceinline__ long long next(const WorkQueue& q, long long limit) {
+    const long long item = base + i;
+    if (i == 0 && item < limit) next_base = take(q);
+    if (++i == per) {
+      base = next_base;
+      i = 0;
+    }
+    return item;
+  }
+};
+
+// Called by one thread of every CTA once the CTA takes no more items.
+__device__ __forceinline__ void finish_queue(const WorkQueue& q) {
+  if (!q.next) return;
+  __threadfence();
+  if (atomicAdd(q.done, 1u) == gridDim.x - 1) {
+    *q.next = 0;
+    *q.done = 0;
+    __threadfence();
+  }
+}
+
 // ---- page-stage ring layout shared by the TMA-fed paged kernels ------------------------
 //
 // Dynamic shared memory: [per-request scan: B int32][ns stages: codes | scales]
@@ -92,6 +158,8 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 struct StageMeta {
   int32_t f0, f1, f2, flags;  // item fields chosen by the kernel; flags bit 1 = page valid
 };
+// flags bit 2: no more items (the consumers leave their loop)
+constexpr int32_t kStageEnd = 4;
 
 struct TmaLayout {
   uint32_t codes_bytes, sf_bytes;  // one page of one tensor

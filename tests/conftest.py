@@ -21,17 +21,22 @@ def has_gpu() -> bool:
         return False
 
 
-@pytest.fixture(params=["ring", "direct"])
+@pytest.fixture(params=["ring", "ring-static", "direct"])
 def append_kernel(request):
     """Run a test once with each append kernel: the TMA ring and the direct-load kernel.
     The library picks one by the size of the call; the host switch
     NVFP4KV_TEST_APPEND_KERNEL (read on every call) overrides that choice, so both kernels
-    meet every case."""
+    meet every case. "ring-static" runs the ring kernels (append, dequantize, materialize)
+    with a fixed share of the work per CTA instead of the shared work counter, so both
+    schedules meet every case too."""
+    import nvfp4_paged_kv_02_gb300 as nv
     old = os.environ.get("NVFP4KV_TEST_APPEND_KERNEL")
-    os.environ["NVFP4KV_TEST_APPEND_KERNEL"] = request.param
+    os.environ["NVFP4KV_TEST_APPEND_KERNEL"] = request.param.split("-")[0]
+    nv.set_dynamic_schedule(request.param != "ring-static")
     try:
         yield request.param
     finally:
+        nv.set_dynamic_schedule(True)
         if old is None:
             os.environ.pop("NVFP4KV_TEST_APPEND_KERNEL", None)
         else:

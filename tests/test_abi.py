@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_e4m3_max(lib):
-    assert lib.nvfp4_abi_version() == 3
+    assert lib.nvfp4_abi_version() == 4
     assert nv.nvfp4_e4m3_max(None) == 448.0
     assert nv.nvfp4_e4m3_max(nv.NVFP44Over6Config(256.0, "MSE")) == 256.0
 
@@ -67,13 +67,14 @@ def cache(ps=16, H=8, D=128, pages=4, data=FAKE, dstride=None, sstride=None):
 
 def append(lib, **kw):
     a = dict(k=FAKE, v=FAKE, dtype=1, nnz=4, H=8, D=128, ks=1024, vs=1024, kc=cache(), vc=cache(),
-             ps=16, layout=0, B=2, k_scale=0.5, v_scale=0.5, recipe=None)
+             ps=16, layout=0, B=2, k_scale=0.5, v_scale=0.5, recipe=None, ws=None)
     a.update(kw)
     return lib.nvfp4_quantize_append_paged(
         ctypes.c_void_p(a["k"]), ctypes.c_void_p(a["v"]), a["dtype"], a["nnz"], a["H"], a["D"],
         a["ks"], a["vs"], ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), a["kc"], a["vc"],
         a["ps"], a["layout"], ctypes.c_void_p(FAKE), 16, ctypes.c_void_p(FAKE), None, a["B"],
-        a["k_scale"], a["v_scale"], a["recipe"], None, None)
+        a["k_scale"], a["v_scale"], a["recipe"], None,
+        None if a["ws"] is None else ctypes.c_void_p(a["ws"]), None)
 
 
 def err(lib):
@@ -122,12 +123,13 @@ def test_empty_append_is_a_no_op(lib):
 
 def dequant(lib, **kw):
     a = dict(kc=cache(), vc=cache(), ps=16, H=8, D=128, layout=1, tdt=0, maxp=4, B=2, out=FAKE,
-             odt=1, L=64)
+             odt=1, L=64, ws=None)
     a.update(kw)
     return lib.nvfp4_dequantize_paged(
         a["kc"], a["vc"], a["ps"], a["H"], a["D"], a["layout"], ctypes.c_void_p(FAKE), a["tdt"],
         a["maxp"], ctypes.c_void_p(FAKE), a["B"], ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE),
-        ctypes.c_void_p(a["out"]), ctypes.c_void_p(FAKE), a["odt"], a["L"], None, None)
+        ctypes.c_void_p(a["out"]), ctypes.c_void_p(FAKE), a["odt"], a["L"], None,
+        None if a["ws"] is None else ctypes.c_void_p(a["ws"]), None)
 
 
 @pytest.mark.parametrize("kw,code,text", [
@@ -149,13 +151,14 @@ def test_empty_dequant_is_a_no_op(lib):
 
 def materialize(lib, **kw):
     a = dict(kc=cache(), vc=cache(), ps=16, H=8, D=128, layout=1, mnp=4, shared=1, B=2, mkl=64,
-             indptr=None, npages=-1, out=FAKE, nout=9, vsf=nv.SF_LINEAR)
+             indptr=None, npages=-1, out=FAKE, nout=9, vsf=nv.SF_LINEAR, ws=None)
     a.update(kw)
     return lib.nvfp4_materialize_fp8(
         a["kc"], a["vc"], a["ps"], a["H"], a["D"], a["layout"], ctypes.c_void_p(FAKE), a["mnp"],
         a["shared"], ctypes.c_void_p(FAKE), a["B"], a["mkl"],
         None if a["indptr"] is None else ctypes.c_void_p(a["indptr"]), a["npages"],
-        ctypes.c_void_p(a["out"]), a["nout"], ctypes.c_void_p(FAKE), 1, a["vsf"], None, None)
+        ctypes.c_void_p(a["out"]), a["nout"], ctypes.c_void_p(FAKE), 1, a["vsf"], None,
+        None if a["ws"] is None else ctypes.c_void_p(a["ws"]), None)
 
 
 @pytest.mark.parametrize("kw,code,text", [
@@ -202,11 +205,12 @@ def test_materializer_run_needs_a_prepared_struct(lib):
     m = nv._Materializer()
     assert lib.nvfp4_materializer_run(
         ctypes.byref(m), cache(), cache(), ctypes.c_void_p(FAKE), 4, ctypes.c_void_p(FAKE), 2, 4,
-        None, -1, ctypes.c_void_p(FAKE), 9, ctypes.c_void_p(FAKE), None, None) == nv.ERR_INVALID_ARG
+        None, -1, ctypes.c_void_p(FAKE), 9, ctypes.c_void_p(FAKE), None, None,
+        None) == nv.ERR_INVALID_ARG
     assert "not prepared" in err(lib)
     assert lib.nvfp4_materializer_run(
         None, cache(), cache(), ctypes.c_void_p(FAKE), 4, ctypes.c_void_p(FAKE), 2, 4, None, -1,
-        ctypes.c_void_p(FAKE), 9, ctypes.c_void_p(FAKE), None, None) == nv.ERR_INVALID_ARG
+        ctypes.c_void_p(FAKE), 9, ctypes.c_void_p(FAKE), None, None, None) == nv.ERR_INVALID_ARG
 
 
 def test_materializer_interleaved_needs_hnd():
@@ -236,7 +240,7 @@ def test_dev_scale_append_rejects_null_scales(lib):
     r = f(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 1, 4, 8, 128, 1024, 1024,
           ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), cache(), cache(), 16, 0,
           ctypes.c_void_p(FAKE), 16, ctypes.c_void_p(FAKE), None, 2, None, ctypes.c_void_p(FAKE),
-          None, None, None)
+          None, None, None, None)
     assert r == nv.ERR_INVALID_ARG and "scale" in err(lib)
 
 
@@ -246,7 +250,8 @@ def kv_quantize(lib, **kw):
     return lib.nvfp4_kv_quantize(ctypes.c_void_p(a["x"]) if a["x"] else None, a["dt"], a["rows"],
                                  a["cols"], a["stride"],
                                  ctypes.c_void_p(a["gs"]) if a["gs"] else None, a["recipe"],
-                                 ctypes.c_void_p(a["out"]), ctypes.c_void_p(FAKE), None, None)
+                                 ctypes.c_void_p(a["out"]), ctypes.c_void_p(FAKE), None, None,
+                                 None)
 
 
 @pytest.mark.parametrize("kw,code,text", [
@@ -289,3 +294,10 @@ def test_kv_dequantize_rejects(lib, kw, code, text):
 def test_empty_contiguous_ops_are_no_ops(lib):
     assert kv_quantize(lib, rows=0) == nv.OK
     assert kv_dequantize(lib, rows=0) == nv.OK
+
+
+def test_a_misaligned_workspace_is_rejected(lib):
+    """The work-distribution workspace must be 8-byte aligned (NULL is allowed)."""
+    assert append(lib, ws=FAKE + 4) == nv.ERR_ALIGNMENT and "workspace" in err(lib)
+    assert dequant(lib, ws=FAKE + 4) == nv.ERR_ALIGNMENT and "workspace" in err(lib)
+    assert materialize(lib, ws=FAKE + 2) == nv.ERR_ALIGNMENT and "workspace" in err(lib)
