@@ -246,6 +246,34 @@ nvfp4_status nvfp4_materialize_fp8_out_pages(int32_t batch_size, int32_t max_kv_
                                              int64_t* out_num_pages,
                                              int32_t* max_pages_per_seq);
 
+/* nvfp4_dequantize_paged for callers that cannot hand the library any device memory. This
+ * entry point has no counterpart on the pages; it is an addition of this library.
+ * The dequantize runs fastest with a work-distribution workspace (NVFP4_WORKSPACE_BYTES).
+ * Some callers cannot provide one: an engine whose memory planner owns every byte of device
+ * memory and hands out no buffers beyond a call's inputs and outputs, and code that must
+ * not call cudaMalloc at all (it runs while the allocator is locked, or must not add
+ * allocations that a memory budget did not plan for). With NULL they would get fixed
+ * shares, about 13 percent slower on a large batch. This variant instead uses a 16-byte
+ * array that the library itself holds in device memory (a file-scope __device__ array:
+ * every GPU that loads the library keeps it until the process exits). It allocates
+ * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ *   Arguments, results and requirements: those of nvfp4_dequantize_paged, without
+ *   `workspace`. The scratch this call needs is those 16 bytes whatever the sizes passed,
+ *   so no size can exceed it; sizes are otherwise checked as for nvfp4_dequantize_paged.
+ *   Set-up: the first call on a device looks up the array's device address on that device
+ *   (cudaGetSymbolAddress, with the device current) and keeps it. Make that first call
+ *   before any stream capture on the device.
+ *   Each call clears the array on `stream` (a 16-byte cudaMemsetAsync) and then launches;
+ *   the kernel leaves it zero again. Every call shares the one array: calls that may
+ *   overlap on the device (other streams, other host threads) race on it and must not be
+ *   issued that way. A call rejected by the argument checks still enqueues the clearing. */
+nvfp4_status nvfp4_dequantize_paged_no_alloc(
+    nvfp4_paged_cache k_cache, nvfp4_paged_cache v_cache, int32_t page_size,
+    int32_t num_kv_heads, int32_t head_dim, int32_t kv_layout, const void* block_tables,
+    int32_t table_dtype, int32_t max_pages_per_request, const int32_t* seq_lens,
+    int32_t batch_size, const float* k_scale, const float* v_scale, void* output_k,
+    void* output_v, int32_t out_dtype, int32_t max_seq_len, int32_t* dev_status, void* stream);
+
 /* Write the active pages of a paged NVFP4 cache as FP8 E4M3
  * ("nvfp4_kv_materialize_fp8"; "NVFP4KVMaterializer.run").
  * Request b's page j (j < ceil(seq_lens[b] / page_size)) goes to output page

@@ -118,6 +118,10 @@ def load() -> ctypes.CDLL:
         L.nvfp4_dequantize_paged.argtypes = [
             _Cache, _Cache, i32, i32, i32, i32, vp, i32, i32, vp, i32, vp, vp, vp, vp, i32, i32,
             vp, vp, vp]
+        L.nvfp4_dequantize_paged_no_alloc.restype = i32
+        L.nvfp4_dequantize_paged_no_alloc.argtypes = [
+            _Cache, _Cache, i32, i32, i32, i32, vp, i32, i32, vp, i32, vp, vp, vp, vp, i32, i32,
+            vp, vp]
         L.nvfp4_materialize_fp8_out_pages.restype = i32
         L.nvfp4_materialize_fp8_out_pages.argtypes = [i32, i32, i32, i64, vp, vp]
         L.nvfp4_materialize_fp8.restype = i32

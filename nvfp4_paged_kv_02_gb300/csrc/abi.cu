@@ -559,6 +559,27 @@ NVFP4_EXPORT nvfp4_status nvfp4_materialize_fp8(
   return launch_materialize(a, static_cast<cudaStream_t>(stream));
 }
 
+NVFP4_EXPORT nvfp4_status nvfp4_dequantize_paged_no_alloc(
+    nvfp4_paged_cache k_cache, nvfp4_paged_cache v_cache, int32_t page_size,
+    int32_t num_kv_heads, int32_t head_dim, int32_t kv_layout, const void* block_tables,
+    int32_t table_dtype, int32_t max_pages_per_request, const int32_t* seq_lens,
+    int32_t batch_size, const float* k_scale, const float* v_scale, void* output_k,
+    void* output_v, int32_t out_dtype, int32_t max_seq_len, int32_t* dev_status, void* stream) {
+  clear_error();
+  void* scratch = nullptr;
+  if (nvfp4_status st = no_alloc_scratch(&scratch)) return st;
+  // the work queue must start at zero: clear it on the stream before the launch
+  const cudaError_t e =
+      cudaMemsetAsync(scratch, 0, NVFP4_WORKSPACE_BYTES, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess)
+    return fail(NVFP4_ERR_CUDA, std::string("nvfp4_dequantize_paged_no_alloc: cudaMemsetAsync: ") +
+                                    cudaGetErrorString(e));
+  return nvfp4_dequantize_paged(k_cache, v_cache, page_size, num_kv_heads, head_dim, kv_layout,
+                                block_tables, table_dtype, max_pages_per_request, seq_lens,
+                                batch_size, k_scale, v_scale, output_k, output_v, out_dtype,
+                                max_seq_len, dev_status, scratch, stream);
+}
+
 constexpr uint32_t kMaterializerMagic = 0x4E564D31u;  // "NVM1"
 
 NVFP4_EXPORT nvfp4_status nvfp4_materializer_prepare(

@@ -12,6 +12,9 @@
 // 16-element block k (8 code bytes + 1 scale byte) into a 32-byte store, so each warp
 // store covers 1 KB of contiguous output; up to eight blocks per thread are loaded before any
 // is decoded to keep enough bytes in flight.
+#include <mutex>
+#include <string>
+
 #include "internal.h"
 #include "pipeline.cuh"
 #include "scan.cuh"
@@ -412,6 +415,45 @@ nvfp4_status launch_dequant(const DequantArgs& a, bool out_bf16, bool bt64, bool
   if (out_bf16)
     return bt64 ? launch_v<true, true>(a, vec256, stream) : launch_v<true, false>(a, vec256, stream);
   return bt64 ? launch_v<false, true>(a, vec256, stream) : launch_v<false, false>(a, vec256, stream);
+}
+
+// ---- scratch of nvfp4_dequantize_paged_no_alloc ------------------------------------------
+//
+// That entry point keeps the work queue of its launches here instead of in a workspace from
+// the caller: one NVFP4_WORKSPACE_BYTES block, which every device that loads the library
+// holds until the process exits, and which every call of that entry point shares. Host code
+// must not pass the array's name to a kernel (on the host it is only a stand-in for the
+// device variable); no_alloc_scratch() looks up its device address once per device.
+static __device__ __align__(256) unsigned char g_no_alloc_scratch[NVFP4_WORKSPACE_BYTES];
+
+nvfp4_status no_alloc_scratch(void** out) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(NVFP4_ERR_CUDA, std::string("nvfp4_dequantize_paged_no_alloc: cudaGetDevice: ") +
+                                    cudaGetErrorString(e));
+  }
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(NVFP4_ERR_UNSUPPORTED, "nvfp4_dequantize_paged_no_alloc: device ordinal above 63");
+  std::lock_guard<std::mutex> lk(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    // the device is current here, so this is the address on that device
+    e = cudaGetSymbolAddress(&p, g_no_alloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      (void)cudaGetLastError();
+      return fail(NVFP4_ERR_CUDA,
+                  std::string("nvfp4_dequantize_paged_no_alloc: cudaGetSymbolAddress: ") +
+                      cudaGetErrorString(e));
+    }
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return NVFP4_OK;
 }
 
 }  // namespace nvfp4

@@ -102,6 +102,9 @@ nvfp4_status launch_kv_dequant(const KvDequantArgs& a, bool out_bf16, bool vec25
 
 nvfp4_status launch_dequant(const DequantArgs& a, bool out_bf16, bool bt64, bool vec256,
                             cudaStream_t stream);
+// Device address (on the current device) of the library-held scratch that
+// nvfp4_dequantize_paged_no_alloc uses as its workspace; looked up once per device.
+nvfp4_status no_alloc_scratch(void** out);
 
 // ---- materialize -------------------------------------------------------------------------
 struct MaterializeArgs {
