@@ -873,9 +873,9 @@ def measure_e2e(step, w: W.Workload, args, total_bytes: int, world: int):
     for e in done:
         e.record(comp)
     read_done.record(comp)
-    lens = np.minimum(w.seq_lens.astype(np.int64), w.max_seq_len)
-    rows = [(b, int(n)) for b, n in enumerate(lens) if n > 0]
-    out_host = None
+    # the dequantized output to read back: every request's rows (paged form), or the two
+    # [rows, cols] outputs (contiguous form); (device view, pinned host view) pairs
+    readback = []
 
     def one(i, readback=False):
         b = i % 2
@@ -899,9 +899,8 @@ def measure_e2e(step, w: W.Workload, args, total_bytes: int, world: int):
         if readback:
             back.wait_stream(comp)
             with torch.cuda.stream(back):
-                for r, n in rows:
-                    out_host[0][r, :n].copy_(step.out_k[r, :n], non_blocking=True)
-                    out_host[1][r, :n].copy_(step.out_v[r, :n], non_blocking=True)
+                for src, dst in readback:
+                    dst.copy_(src, non_blocking=True)
                 read_done.record(back)
 
     def windows(readback=False):
@@ -947,26 +946,39 @@ def measure_e2e(step, w: W.Workload, args, total_bytes: int, world: int):
     torch.cuda.synchronize(dev)
     link = hk.numel() * hk.element_size() / (a.elapsed_time(z) * 1e-3) / 1e9
 
-    out_host = tuple(torch.empty(step.out_k.shape, dtype=step.out_k.dtype, pin_memory=True)
-                     for _ in range(2))
+    if isinstance(step, ContigStep):
+        for o in step.out:
+            readback.append((o, torch.empty(o.shape, dtype=o.dtype, pin_memory=True)))
+    else:
+        lens = np.minimum(w.seq_lens.astype(np.int64), w.max_seq_len)
+        host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+                for o in (step.out_k, step.out_v)]
+        for r, n in enumerate(lens):
+            if n > 0:
+                readback.append((step.out_k[r, :n], host[0][r, :n]))
+                readback.append((step.out_v[r, :n], host[1][r, :n]))
     wins_rb = windows(readback=True)
     ms_rb = max_over_ranks(float(np.median(wins_rb)), dev)
-    d2h_rb = 2 * int(lens.sum()) * w.H * w.D * step.out_k.element_size() + 12
+    d2h_rb = sum(src.numel() * src.element_size() for src, _ in readback) + 12
     step.k, step.v = bufs[0]
     return {"value": world * total_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 12, "ms_per_step": ms,
             "value_counts": "appended K/V rows copied in, the step's summary (two global "
                             "scales and the status word) read back",
-            "resident_on_device": ["paged K/V cache (codes and block scales)",
-                                   "dequantized K/V (out_k, out_v)",
-                                   "FP8 copy and fp8_block_tables"],
+            "resident_on_device": (["NVFP4 codes and block scales of K and V",
+                                    "dequantized K and V"] if isinstance(step, ContigStep)
+                                   else ["paged K/V cache (codes and block scales)",
+                                         "dequantized K/V (out_k, out_v)",
+                                         "FP8 copy and fp8_block_tables"]),
             "pipelined": "copies of step i+1 overlap the compute of step i (two buffers)",
             "windows_ms_per_step": wins, "host_to_device_gbs": link, "clocks": clk,
             "with_dequant_readback": {
                 "value": world * total_bytes / (ms_rb * 1e-3) / 1e9, "unit": "GB/s",
                 "ms_per_step": ms_rb, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h_rb,
-                "reads_back": "every request's dequantized K and V rows (rows < seq_lens) and "
-                              "the summary",
+                "reads_back": ("both dequantized [rows, cols] outputs and the summary"
+                               if isinstance(step, ContigStep) else
+                               "every request's dequantized K and V rows (rows < seq_lens) and "
+                               "the summary"),
                 "windows_ms_per_step": wins_rb}}
 
 

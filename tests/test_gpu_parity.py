@@ -40,6 +40,26 @@ def test_named_workload(name):
     PL.assert_same(g, o, name)
 
 
+def test_every_kernel_leaves_its_workspace_zero():
+    """The ring kernels take work from a counter in the stream's workspace; the last CTA to
+    finish sets it back to zero, so the next call starts from zero without a memset. After
+    the append, dequant and materialize of a named workload (and the contiguous quantize),
+    every workspace the binding handed out must hold zero."""
+    import nvfp4_paged_kv_02_gb300 as nv
+    if not nv._dynamic_schedule:
+        pytest.skip("fixed shares use no workspace")
+    w = W.NAMED["materialize"]()
+    g = PL.run_gpu(w)
+    o = PL.run_oracle(w)
+    PL.assert_same(g, o, "workspace")
+    x = torch.randn((4096, 1024), generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
+    nv.nvfp4_kv_quantize(x.cuda(), 0.01)
+    torch.cuda.synchronize()
+    assert nv._workspaces, "no workspace was used"
+    for key, ws in nv._workspaces.items():
+        assert int(ws.abs().sum()) == 0, (key, ws.tolist())
+
+
 CASES = []
 for seed, (layout, dt, ps, D, recipe, bt) in enumerate([
     (W.NHD, torch.bfloat16, 16, 128, R_STD, np.int32),
