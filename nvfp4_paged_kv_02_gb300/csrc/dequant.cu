@@ -178,6 +178,14 @@ __global__ void __launch_bounds__(kTmaThreads, 4) dequant_tma_kernel(const Dequa
   const int64_t items = 2 * static_cast<int64_t>(s_cum[a.B - 1]);
 
   const WorkQueue q = work_queue(a.workspace);
+  // With the work queue the last items (at most two per CTA) are handed out as two halves
+  // each -- heads [0, H/2) and [H/2, H) of an HND page, slots [0, ps/2) and [ps/2, ps) of an
+  // NHD one -- so that the last wave ends more evenly. Units below full_items are whole
+  // pages; each item after them is two units.
+  const int64_t full_items =
+      (q.next && a.split) ? max(static_cast<int64_t>(0), items - 2 * static_cast<int64_t>(gridDim.x))
+                          : items;
+  const int64_t units = full_items + 2 * (items - full_items);
   if (warp == kConsumerWarps) {
     // producer: lane 0 takes the items and issues, the warp stays converged
     int s = 0;
@@ -187,10 +195,16 @@ __global__ void __launch_bounds__(kTmaThreads, 4) dequant_tma_kernel(const Dequa
     for (;; s = (s + 1 == ns) ? 0 : s + 1, round += (s == 0)) {
       // the next item and its source page, resolved while the consumers still work on the
       // stage it will use
-      long long item = 0;
-      if (lane == 0) item = cur.next(q, items);
-      item = __shfl_sync(0xFFFFFFFFu, item, 0);
-      const bool end = item >= items;
+      long long unit = 0;
+      if (lane == 0) unit = cur.next(q, units);
+      unit = __shfl_sync(0xFFFFFFFFu, unit, 0);
+      const bool end = unit >= units;
+      long long item = unit;
+      int part = 0;  // 0: the whole page; 1, 2: its first or second half
+      if (unit >= full_items) {
+        item = full_items + ((unit - full_items) >> 1);
+        part = 1 + static_cast<int>((unit - full_items) & 1);
+      }
       StageMeta m{0, 0, 0, kStageEnd};
       int64_t page = 0;
       if (lane == 0 && !end) {
@@ -207,7 +221,7 @@ __global__ void __launch_bounds__(kTmaThreads, 4) dequant_tma_kernel(const Dequa
         m.f0 = b;
         m.f1 = t0;
         m.f2 = min(ps, len - t0);
-        m.flags = kv | (valid ? 2 : 0);
+        m.flags = kv | (valid ? 2 : 0) | (part << 3);
       }
       bool ok = true;
       if (lane == 0) ok = mbar_wait(empty + s, (round & 1u) ^ 1u, a.pipe.wait_limit) && !*s_abort;
@@ -229,9 +243,13 @@ __global__ void __launch_bounds__(kTmaThreads, 4) dequant_tma_kernel(const Dequa
           const uint8_t* sf = kv ? a.vc.sf : a.kc.sf;
           const int64_t dps = kv ? a.vc.data_page_stride : a.kc.data_page_stride;
           const int64_t sps = kv ? a.vc.sf_page_stride : a.kc.sf_page_stride;
-          mbar_arrive_expect_tx(full + s, L.codes_bytes + L.sf_bytes);
-          bulk_g2s(st, data + page * dps, L.codes_bytes, full + s);
-          bulk_g2s(st + L.sf_off, sf + page * sps, L.sf_bytes, full + s);
+          // a half page is the first or second half of the page's codes and of its scales
+          const uint32_t cb = part ? L.codes_bytes / 2 : L.codes_bytes;
+          const uint32_t sb = part ? L.sf_bytes / 2 : L.sf_bytes;
+          const int64_t off_c = part == 2 ? cb : 0, off_s = part == 2 ? sb : 0;
+          mbar_arrive_expect_tx(full + s, cb + sb);
+          bulk_g2s(st, data + page * dps + off_c, cb, full + s);
+          bulk_g2s(st + L.sf_off, sf + page * sps + off_s, sb, full + s);
         } else {
           if (!end) flag(a.status, NVFP4_DEV_BAD_PAGE);
           mbar_arrive(full + s);
@@ -266,27 +284,34 @@ __global__ void __launch_bounds__(kTmaThreads, 4) dequant_tma_kernel(const Dequa
                       (static_cast<int64_t>(m.f0) * L_out + m.f1) * row_bytes;
         const float gs = (m.flags & 1) ? gs_v : gs_k;
         const int32_t ntok = m.f2;
+        const int part = (m.flags >> 3) & 3;
         if (a.layout == NVFP4_NHD) {
-          // the page holds [slot, head, block]: the same order as the output run
-          const int32_t nblk = ntok * row_blocks;
+          // the page holds [slot, head, block]: the same order as the output run (a half page:
+          // slots [lo, lo + ps/2))
+          const int32_t lo = part == 2 ? ps / 2 : 0;
+          const int32_t n = max(0, min(ntok - lo, part ? ps / 2 : ps));
+          const int32_t nblk = n * row_blocks;
+          uint8_t* ob_h = ob + static_cast<int64_t>(lo) * row_bytes;
 #pragma unroll 4
           for (int32_t k = ct; k < nblk; k += kConsumers) {
             const uint2 codes = *reinterpret_cast<const uint2*>(st + 8 * k);
-            st_256(ob + static_cast<int64_t>(k) * 32, decode_block<OUT_BF16>(codes, sfp[k], gs));
+            st_256(ob_h + static_cast<int64_t>(k) * 32, decode_block<OUT_BF16>(codes, sfp[k], gs));
           }
         } else {
           // the page holds [head, slot, block]: read it in that order (no shared-memory
-          // bank conflicts); each group of nb lanes still writes a contiguous output row
-          const int32_t page_blocks = a.H * ps * a.nb;
+          // bank conflicts); each group of nb lanes still writes a contiguous output row (a half
+          // page: heads [h0, h0 + H/2))
+          const int32_t h0 = part == 2 ? a.H / 2 : 0;
+          const int32_t page_blocks = (part ? a.H / 2 : a.H) * ps * a.nb;
 #pragma unroll 4
           for (int32_t k = ct; k < page_blocks; k += kConsumers) {
-            const int32_t hs = div_q32(k, a.div_nb);  // h * ps + slot
+            const int32_t hs = div_q32(k, a.div_nb);  // (h - h0) * ps + slot
             const int32_t blk = k - hs * a.nb;
             const int32_t h = div_q32(hs, a.div_ps);
             const int32_t slot = hs - h * ps;
             if (slot >= ntok) continue;
             const uint2 codes = *reinterpret_cast<const uint2*>(st + 8 * k);
-            const int32_t o = (slot * a.H + h) * a.nb + blk;
+            const int32_t o = (slot * a.H + h0 + h) * a.nb + blk;
             st_256(ob + static_cast<int64_t>(o) * 32, decode_block<OUT_BF16>(codes, sfp[k], gs));
           }
         }
@@ -386,12 +411,17 @@ nvfp4_status launch_tma(const DequantArgs& a, uint32_t codes_bytes, uint32_t sf_
                         cudaStream_t stream) {
   const auto kern = dequant_tma_kernel<OUT_BF16, BT64>;
   const TmaLayout L = tma_layout(a.B, codes_bytes, sf_bytes, stages_for(codes_bytes, sf_bytes, 48u * 1024u));
+  // halves of a page can be bulk-copied when the split dimension is even and each half of
+  // the codes and of the scales is a whole number of 16-byte units
+  DequantArgs b = a;
+  const int32_t split_dim = a.layout == NVFP4_NHD ? a.ps : a.H;
+  b.split = split_dim % 2 == 0 && (codes_bytes / 2) % 16 == 0 && (sf_bytes / 2) % 16 == 0;
   const nvfp4_status st =
       set_dynamic_smem(reinterpret_cast<const void*>(kern), L.total, "nvfp4_dequantize_paged");
   if (st != NVFP4_OK) return st;
   const int grid =
       sm_count() * blocks_per_sm(reinterpret_cast<const void*>(kern), kTmaThreads, L.total);
-  kern<<<grid, kTmaThreads, L.total, stream>>>(a, L);
+  kern<<<grid, kTmaThreads, L.total, stream>>>(b, L);
   return check_launch("nvfp4_dequantize_paged");
 }
 

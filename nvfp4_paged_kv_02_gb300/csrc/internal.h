@@ -87,6 +87,7 @@ struct DequantArgs {
   PipeTest pipe;
   int32_t* status;
   void* workspace;  // NVFP4_WORKSPACE_BYTES (dynamic schedule of the ring kernel) or null
+  int32_t split;    // the ring kernel may hand out halves of a page (set at launch)
 };
 // Contiguous dequantize (nvfp4_kv_dequantize): block k of the flattened [rows, cols] codes
 // (8 bytes at codes + 8k, scale byte sf[k]) becomes 16 outputs at out + 32k bytes.
