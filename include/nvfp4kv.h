@@ -37,7 +37,7 @@
  *     NULL the kernel ORs the matching NVFP4_DEV_* bit into *dev_status (device memory,
  *     one int32 the caller zeroes).
  *   - Work distribution (`workspace`, the last-but-one argument of the append, dequantize,
- *     materialize and contiguous-quantize calls): NULL, or NVFP4_WORKSPACE_BYTES of device
+ *     materialize and contiguous quantize and dequantize calls): NULL, or NVFP4_WORKSPACE_BYTES of device
  *     memory, 8-byte aligned, that is zero before its first use. With it, the persistent
  *     CTAs of the bulk-copy kernels take work items from a counter there as they free up
  *     (CTAs on SMs that run ahead take more); the kernel sets it back to zero before it
@@ -58,7 +58,7 @@
 extern "C" {
 #endif
 
-#define NVFP4KV_ABI_VERSION 4
+#define NVFP4KV_ABI_VERSION 5
 
 /* Bytes of the optional `workspace` of the bulk-copy kernels (see the conventions). */
 #define NVFP4_WORKSPACE_BYTES 16
@@ -391,10 +391,16 @@ nvfp4_status nvfp4_kv_quantize(const void* input, int32_t dtype, int64_t rows, i
  *   global_scale device float.
  *   out          device [rows, cols] of out_dtype (NVFP4_F16 or NVFP4_BF16), contiguous,
  *                16-byte aligned.
- * Requirements: cols % 16 == 0, cols > 0, rows >= 0. */
+ *   dev_status   NULL or a device int32: NVFP4_DEV_TIMEOUT if a wait of the bulk-copy
+ *                kernel for a shared-memory stage ran out.
+ *   workspace    NULL or the work-distribution workspace (see the conventions).
+ * Requirements: cols % 16 == 0, cols > 0, rows >= 0. With fp4 and sf 16-byte aligned, out
+ * 32-byte aligned and at least 16384 elements, the codes and scales are read in bulk copies
+ * of 1024 blocks; otherwise each thread loads its blocks directly. */
 nvfp4_status nvfp4_kv_dequantize(const uint8_t* fp4, const uint8_t* sf, int64_t rows,
                                  int32_t cols, const float* global_scale, void* out,
-                                 int32_t out_dtype, int32_t* dev_status, void* stream);
+                                 int32_t out_dtype, int32_t* dev_status, void* workspace,
+                                 void* stream);
 
 /* Pack a resolved recipe into one int64, for logs and repro tooling
  * ("flashinfer.quantization" index, "NVFP4 4over6 Recipes": nvfp4_4over6_code and its

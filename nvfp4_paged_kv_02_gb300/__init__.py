@@ -140,7 +140,7 @@ def load() -> ctypes.CDLL:
         L.nvfp4_kv_quantize.restype = i32
         L.nvfp4_kv_quantize.argtypes = [vp, i32, i64, i32, i64, vp, vp, vp, vp, vp, vp, vp]
         L.nvfp4_kv_dequantize.restype = i32
-        L.nvfp4_kv_dequantize.argtypes = [vp, vp, i64, i32, vp, vp, i32, vp, vp]
+        L.nvfp4_kv_dequantize.argtypes = [vp, vp, i64, i32, vp, vp, i32, vp, vp, vp]
         _lib = L
         return L
 
@@ -540,7 +540,7 @@ def nvfp4_kv_dequantize(fp4_data: torch.Tensor, block_scales: torch.Tensor, glob
     gs = _scale_tensor(global_scale, fp4_data.device)
     _check("nvfp4_kv_dequantize", load().nvfp4_kv_dequantize(
         _ptr(fp4_data), _ptr(block_scales), rows, cols, _ptr(gs), _ptr(out),
-        _dtype_code(out.dtype), _ptr(dev_status), _stream(fp4_data.device)))
+        _dtype_code(out.dtype), _ptr(dev_status), *_ws_stream(fp4_data.device)))
     return out
 
 

@@ -390,9 +390,9 @@ NVFP4_EXPORT nvfp4_status nvfp4_kv_dequantize(const uint8_t* fp4, const uint8_t*
                                               int64_t rows, int32_t cols,
                                               const float* global_scale, void* out,
                                               int32_t out_dtype, int32_t* dev_status,
-                                              void* stream) {
+                                              void* workspace, void* stream) {
   clear_error();
-  (void)dev_status;  // no device-held indices: nothing to report
+  if (nvfp4_status st = check_workspace("nvfp4_kv_dequantize", workspace)) return st;
   if (out_dtype != NVFP4_F16 && out_dtype != NVFP4_BF16)
     return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_kv_dequantize: out_dtype must be NVFP4_F16 or NVFP4_BF16");
   if (cols <= 0 || cols % 16 != 0)
@@ -409,6 +409,9 @@ NVFP4_EXPORT nvfp4_status nvfp4_kv_dequantize(const uint8_t* fp4, const uint8_t*
   a.blocks = rows * (cols / 16);
   a.gs = global_scale;
   a.out = static_cast<uint8_t*>(out);
+  a.status = dev_status;
+  a.pipe = pipe_test_from_env();
+  a.workspace = workspace;
   return launch_kv_dequant(a, out_dtype == NVFP4_BF16, aligned(out, 32),
                            static_cast<cudaStream_t>(stream));
 }

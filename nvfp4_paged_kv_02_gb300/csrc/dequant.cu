@@ -371,6 +371,138 @@ __global__ void __launch_bounds__(kKvThreads) kv_dequant_kernel(const KvDequantA
   }
 }
 
+// The contiguous form through the same kind of ring as the paged one: a work item is a
+// chunk of kKvChunk consecutive blocks (8 KB of codes and 1 KB of scales, one bulk copy each;
+// 32 KB of 16-bit output), so that the reads reach HBM as long runs instead of each warp's
+// 256-byte load. The blocks after the last whole chunk (fewer than kKvChunk) are decoded
+// straight from global memory by the consumer threads, one block each, before the ring.
+// Needs 16-byte aligned codes and scales and a 32-byte aligned output.
+constexpr int32_t kKvChunk = 1024;
+
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(kTmaThreads, 4) kv_dequant_tma_kernel(const KvDequantArgs a,
+                                                                     const TmaLayout L) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* stages = smem + L.stages_off;
+  StageMeta* meta = reinterpret_cast<StageMeta*>(smem + L.meta_off);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars_off);
+  uint64_t* empty = full + L.ns;
+  volatile int32_t* s_abort = reinterpret_cast<int32_t*>(smem + L.misc_off);
+  volatile uint32_t* s_issued = reinterpret_cast<uint32_t*>(smem + L.misc_off + 4);
+  const int ns = L.ns;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ns; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, kConsumerWarps);
+      s_issued[s] = 0;
+    }
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int64_t chunks = a.blocks / kKvChunk;
+  const WorkQueue q = work_queue(a.workspace);
+  if (warp == kConsumerWarps) {
+    // producer: lane 0 takes the chunks and issues, the warp stays converged
+    int s = 0;
+    uint32_t round = 0;  // how many times stage s has been used before
+    ItemCursor cur;
+    if (lane == 0) cur.init(q, 1);
+    for (;; s = (s + 1 == ns) ? 0 : s + 1, round += (s == 0)) {
+      long long item = 0;
+      if (lane == 0) item = cur.next(q, chunks);
+      item = __shfl_sync(0xFFFFFFFFu, item, 0);
+      const bool end = item >= chunks;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(empty + s, (round & 1u) ^ 1u, a.pipe.wait_limit) && !*s_abort;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) {
+        if (lane == 0) {
+          *s_abort = 1;
+          flag(a.status, NVFP4_DEV_TIMEOUT);
+        }
+        break;
+      }
+      // (test control: withhold the first stage so that the consumers' wait expires)
+      if (lane == 0 && (end || !(a.pipe.stall && round == 0 && s == 0))) {
+        // the chunk index in two halves (f0 low, f1 high)
+        meta[s] = StageMeta{static_cast<int32_t>(item & 0xFFFFFFFFll),
+                            static_cast<int32_t>(item >> 32), 0, end ? kStageEnd : 2};
+        if (!end) {
+          uint8_t* st = stages + static_cast<uint32_t>(s) * L.stage_bytes;
+          mbar_arrive_expect_tx(full + s, 9u * kKvChunk);
+          bulk_g2s(st, a.codes + item * (8 * kKvChunk), 8u * kKvChunk, full + s);
+          bulk_g2s(st + L.sf_off, a.sf + item * kKvChunk, static_cast<uint32_t>(kKvChunk), full + s);
+        } else {
+          mbar_arrive(full + s);
+        }
+        s_issued[s] = round + 1;
+      }
+      __syncwarp();
+      if (end) break;
+    }
+  } else {
+    const int ct = threadIdx.x;  // 0 .. kConsumers-1
+    const float gs = __ldg(a.gs);
+    // the blocks after the last whole chunk
+    for (int64_t b = chunks * kKvChunk + static_cast<int64_t>(blockIdx.x) * kConsumers + ct;
+         b < a.blocks; b += static_cast<int64_t>(gridDim.x) * kConsumers) {
+      const uint2 codes = __ldg(reinterpret_cast<const uint2*>(a.codes) + b);
+      st_256(a.out + b * 32, decode_block<OUT_BF16>(codes, __ldg(a.sf + b), gs));
+    }
+    int s = 0;
+    uint32_t round = 0;  // how many times stage s has been used before
+    for (;; s = (s + 1 == ns) ? 0 : s + 1, round += (s == 0)) {
+      if (*s_abort || !mbar_wait(full + s, round & 1u, a.pipe.wait_limit)) {
+        if (lane == 0) {
+          *s_abort = 1;
+          flag(a.status, NVFP4_DEV_TIMEOUT);
+        }
+        break;
+      }
+      const StageMeta m = meta[s];
+      if (m.flags & kStageEnd) break;
+      const int64_t item = static_cast<int64_t>(static_cast<uint32_t>(m.f0)) |
+                           (static_cast<int64_t>(m.f1) << 32);
+      const uint8_t* st = stages + static_cast<uint32_t>(s) * L.stage_bytes;
+      uint8_t* ob = a.out + item * (32 * kKvChunk);
+#pragma unroll
+      for (int32_t k = ct; k < kKvChunk; k += kConsumers) {
+        const uint2 codes = *reinterpret_cast<const uint2*>(st + 8 * k);
+        st_256(ob + static_cast<int64_t>(k) * 32,
+               decode_block<OUT_BF16>(codes, st[L.sf_off + k], gs));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + s);
+    }
+  }
+  // no copy may still be landing in this CTA's shared memory when it exits
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ns; ++s)
+      if (s_issued[s] > 0) mbar_wait(full + s, (s_issued[s] - 1) & 1u, a.pipe.wait_limit);
+    finish_queue(q);
+  }
+}
+
+template <bool OUT_BF16>
+nvfp4_status launch_kv_tma(const KvDequantArgs& a, cudaStream_t stream) {
+  const auto kern = kv_dequant_tma_kernel<OUT_BF16>;
+  const uint32_t cb = 8u * kKvChunk, sb = static_cast<uint32_t>(kKvChunk);
+  const TmaLayout L = tma_layout(0, cb, sb, stages_for(cb, sb, 48u * 1024u));
+  const nvfp4_status st =
+      set_dynamic_smem(reinterpret_cast<const void*>(kern), L.total, "nvfp4_kv_dequantize");
+  if (st != NVFP4_OK) return st;
+  const int64_t chunks = a.blocks / kKvChunk;
+  const int64_t cap = static_cast<int64_t>(sm_count()) *
+                      blocks_per_sm(reinterpret_cast<const void*>(kern), kTmaThreads, L.total);
+  const int grid = static_cast<int>(chunks < cap ? chunks : cap);
+  kern<<<grid, kTmaThreads, L.total, stream>>>(a, L);
+  return check_launch("nvfp4_kv_dequantize");
+}
+
 template <bool OUT_BF16, bool VEC256>
 nvfp4_status launch_kv(const KvDequantArgs& a, cudaStream_t stream) {
   const auto kern = kv_dequant_kernel<OUT_BF16, VEC256>;
@@ -436,6 +568,9 @@ nvfp4_status launch_v(const DequantArgs& a, bool vec256, cudaStream_t s) {
 
 nvfp4_status launch_kv_dequant(const KvDequantArgs& a, bool out_bf16, bool vec256,
                                cudaStream_t stream) {
+  const auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  if (vec256 && al16(a.codes) && al16(a.sf) && a.blocks >= kKvChunk)
+    return out_bf16 ? launch_kv_tma<true>(a, stream) : launch_kv_tma<false>(a, stream);
   if (out_bf16) return vec256 ? launch_kv<true, true>(a, stream) : launch_kv<true, false>(a, stream);
   return vec256 ? launch_kv<false, true>(a, stream) : launch_kv<false, false>(a, stream);
 }

@@ -97,6 +97,9 @@ struct KvDequantArgs {
   int64_t blocks;  // rows * cols / 16
   const float* gs;
   uint8_t* out;
+  int32_t* status;  // may be null
+  PipeTest pipe;
+  void* workspace;  // null: fixed shares
 };
 nvfp4_status launch_kv_dequant(const KvDequantArgs& a, bool out_bf16, bool vec256,
                                cudaStream_t stream);

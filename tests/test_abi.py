@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_e4m3_max(lib):
-    assert lib.nvfp4_abi_version() == 4
+    assert lib.nvfp4_abi_version() == 5
     assert nv.nvfp4_e4m3_max(None) == 448.0
     assert nv.nvfp4_e4m3_max(nv.NVFP44Over6Config(256.0, "MSE")) == 256.0
 
@@ -271,11 +271,12 @@ def test_kv_quantize_rejects(lib, kw, code, text):
 
 
 def kv_dequantize(lib, **kw):
-    a = dict(fp4=FAKE, rows=4, cols=128, gs=FAKE, out=FAKE, odt=1)
+    a = dict(fp4=FAKE, rows=4, cols=128, gs=FAKE, out=FAKE, odt=1, ws=None)
     a.update(kw)
     return lib.nvfp4_kv_dequantize(ctypes.c_void_p(a["fp4"]), ctypes.c_void_p(FAKE), a["rows"],
                                    a["cols"], ctypes.c_void_p(a["gs"]) if a["gs"] else None,
-                                   ctypes.c_void_p(a["out"]), a["odt"], None, None)
+                                   ctypes.c_void_p(a["out"]), a["odt"], None,
+                                   ctypes.c_void_p(a["ws"]) if a["ws"] else None, None)
 
 
 @pytest.mark.parametrize("kw,code,text", [
@@ -301,3 +302,4 @@ def test_a_misaligned_workspace_is_rejected(lib):
     assert append(lib, ws=FAKE + 4) == nv.ERR_ALIGNMENT and "workspace" in err(lib)
     assert dequant(lib, ws=FAKE + 4) == nv.ERR_ALIGNMENT and "workspace" in err(lib)
     assert materialize(lib, ws=FAKE + 2) == nv.ERR_ALIGNMENT and "workspace" in err(lib)
+    assert kv_dequantize(lib, ws=FAKE + 4) == nv.ERR_ALIGNMENT and "workspace" in err(lib)

@@ -3,7 +3,8 @@ nvfp4_kv_dequantize) through the C ABI against the CPU oracle, bit-exact on the 
 codes, the scale bytes and the dequantized fp16/bf16 values. Sizes span several pipeline
 tiles with a ragged tail, strided input rows, rows too long for a shared-memory stage (the
 direct-load kernel), the recipes and both dtypes. Every test runs once with each quantize
-kernel (the TMA ring and the direct-load kernel)."""
+kernel (the TMA ring and the direct-load kernel); the dequantize's two kernels are chosen
+by alignment and size, and one test runs each."""
 import numpy as np
 import pytest
 import torch
@@ -70,6 +71,37 @@ def test_kv_quantize_dequantize(seed, rows, cols, pad, recipe, dtype):
         y = nv.nvfp4_kv_dequantize(fp4, sf, g, out_dt)
         want = O.kv_dequantize(o_codes, o_sf, gs, out_dt == torch.bfloat16)
         assert np.array_equal(W.bits16(y.cpu()), want), out_dt
+
+
+@pytest.mark.parametrize("rows,cols", [(64, 256), (257, 1024), (2049, 48), (5, 16384)])
+def test_kv_dequantize_each_kernel(rows, cols):
+    """The dequantize reads aligned codes and scales of at least 1024 blocks through its
+    bulk-copy ring (the blocks after the last whole chunk of 1024 directly), and anything
+    else with direct loads: scales one byte off a 16-byte boundary, or an output 16 bytes
+    off a 32-byte boundary (16-byte stores). Each must match the oracle."""
+    import nvfp4_paged_kv_02_gb300 as nv
+    dev = torch.device("cuda")
+    x = _input(4242 + rows, rows, cols, torch.bfloat16)
+    gs = float(np.float32(float(x.float().abs().max()) / 2688.0))
+    c, s = O.kv_quantize(W.bits16(x), True, gs, None)
+    g = torch.tensor([gs], dtype=torch.float32, device=dev)
+    fp4 = torch.from_numpy(c).to(dev)
+    sf = torch.from_numpy(s).to(dev)
+    sf_buf = torch.zeros(s.size + 16, dtype=torch.uint8, device=dev)
+    sf_off = sf_buf[1:1 + s.size].view(rows, cols // 16)  # 1 byte past an aligned base
+    sf_off.copy_(sf)
+    for out_dt in (torch.bfloat16, torch.float16):
+        want = O.kv_dequantize(c, s, gs, out_dt == torch.bfloat16)
+        out_buf = torch.full((rows * cols + 16,), float("nan"), dtype=out_dt, device=dev)
+        shifted = out_buf[8:8 + rows * cols].view(rows, cols)  # 16 bytes past a 32-byte base
+        for name, scales, out in (("ring", sf, None), ("scales off 16 B", sf_off, None),
+                                  ("output off 32 B", sf, shifted)):
+            st = torch.zeros(1, dtype=torch.int32, device=dev)
+            y = nv.nvfp4_kv_dequantize(fp4, scales, g, out_dt, out=out, dev_status=st)
+            torch.cuda.synchronize()
+            assert int(st.item()) == 0, name
+            assert np.array_equal(W.bits16(y.cpu()), want), (name, out_dt)
+        assert bool(out_buf[:8].isnan().all()) and bool(out_buf[8 + rows * cols:].isnan().all())
 
 
 def test_kv_quantize_leading_dims_and_out():

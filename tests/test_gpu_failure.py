@@ -3,7 +3,8 @@
 Every shared-memory stage wait in the TMA-fed kernels is bounded. Here the host makes a
 wait run out: NVFP4KV_TEST_STALL_PIPELINE=1 makes each CTA's producer withhold its first
 stage (a barrier nothing completes) and shortens the wait limit. The contiguous quantize
-runs the append's pipeline and is checked the same way. The call must come back
+runs the append's pipeline and the contiguous dequantize a ring of its own; both are checked
+the same way. The call must come back
 on its own with NVFP4_DEV_TIMEOUT set, and the CUDA context must stay usable: the same call
 without the switch then matches the CPU oracle.
 """
@@ -53,7 +54,7 @@ def test_stalled_pipelines_report_timeout_and_recover(stall_env):
     vd, vs = kd.clone(), ks.clone()
     g = torch.tensor([0.01], dtype=torch.float32, device=dev)
     r = PL.gpu_recipe(w.recipe)
-    for op in ("append", "dequant", "materialize", "kv_quantize"):
+    for op in ("append", "dequant", "materialize", "kv_quantize", "kv_dequantize"):
         st = torch.zeros(1, dtype=torch.int32, device=dev)
         if op == "append":
             nv.nvfp4_quantize_append_paged(w.k.to(dev), w.v.to(dev), t(w.batch_indices),
@@ -66,8 +67,12 @@ def test_stalled_pipelines_report_timeout_and_recover(stall_env):
         elif op == "materialize":
             nv.nvfp4_materialize_fp8(kd, vd, ks, vs, t(w.mat_block_tables), t(w.seq_lens),
                                      w.max_kv_len, True, kv_layout="HND", dev_status=st)
-        else:  # the contiguous quantize shares the append's pipeline
+        elif op == "kv_quantize":  # the contiguous quantize shares the append's pipeline
             nv.nvfp4_kv_quantize(w.k.to(dev).reshape(w.nnz, -1), g, r, dev_status=st)
+        else:  # nnz rows of 1024 elements: whole chunks of the contiguous dequantize's ring
+            codes = torch.zeros((w.nnz, w.H * w.D // 2), dtype=torch.uint8, device=dev)
+            scales = torch.zeros((w.nnz, w.H * w.D // 16), dtype=torch.uint8, device=dev)
+            nv.nvfp4_kv_dequantize(codes, scales, g, torch.bfloat16, dev_status=st)
         torch.cuda.synchronize()
         assert int(st.item()) & nv.DEV_TIMEOUT, (op, int(st.item()))
     # the context is still usable: a normal run matches the oracle

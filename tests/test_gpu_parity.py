@@ -43,7 +43,8 @@ def test_named_workload(name):
 def test_every_kernel_leaves_its_workspace_zero():
     """The ring kernels take work from a counter in the stream's workspace; the last CTA to
     finish sets it back to zero, so the next call starts from zero without a memset. After
-    the append, dequant and materialize of a named workload (and the contiguous quantize),
+    the append, dequant and materialize of a named workload (and the contiguous quantize and
+    dequantize),
     every workspace the binding handed out must hold zero."""
     import nvfp4_paged_kv_02_gb300 as nv
     if not nv._dynamic_schedule:
@@ -53,7 +54,8 @@ def test_every_kernel_leaves_its_workspace_zero():
     o = PL.run_oracle(w)
     PL.assert_same(g, o, "workspace")
     x = torch.randn((4096, 1024), generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
-    nv.nvfp4_kv_quantize(x.cuda(), 0.01)
+    fp4, sf = nv.nvfp4_kv_quantize(x.cuda(), 0.01)
+    nv.nvfp4_kv_dequantize(fp4, sf, 0.01)
     torch.cuda.synchronize()
     assert nv._workspaces, "no workspace was used"
     for key, ws in nv._workspaces.items():
