@@ -877,7 +877,7 @@ def measure_e2e(step, w: W.Workload, args, total_bytes: int, world: int):
     # [rows, cols] outputs (contiguous form); (device view, pinned host view) pairs
     readback = []
 
-    def one(i, readback=False):
+    def one(i, read_back=False):
         b = i % 2
         k, v = bufs[b]
         with torch.cuda.stream(copy):
@@ -886,7 +886,7 @@ def measure_e2e(step, w: W.Workload, args, total_bytes: int, world: int):
             v.copy_(hv, non_blocking=True)
             copied[b].record(copy)
         comp.wait_event(copied[b])
-        if readback:
+        if read_back:
             comp.wait_event(read_done)  # the previous step's outputs have been read back
         step.k, step.v = k, v
         step.run()
@@ -896,16 +896,16 @@ def measure_e2e(step, w: W.Workload, args, total_bytes: int, world: int):
         sm[2] = step.status[0].float()
         res[b].copy_(sm, non_blocking=True)
         done[b].record(comp)
-        if readback:
+        if read_back:
             back.wait_stream(comp)
             with torch.cuda.stream(back):
                 for src, dst in readback:
                     dst.copy_(src, non_blocking=True)
                 read_done.record(back)
 
-    def windows(readback=False):
+    def windows(read_back=False):
         for i in range(2):
-            one(i, readback)
+            one(i, read_back)
         torch.cuda.synchronize(dev)
         a = torch.cuda.Event(enable_timing=True)
         z = torch.cuda.Event(enable_timing=True)
@@ -918,7 +918,7 @@ def measure_e2e(step, w: W.Workload, args, total_bytes: int, world: int):
             a.record(comp)
             copy.wait_stream(comp)  # the timed copies start after the start event
             for i in range(n):
-                one(i, readback)
+                one(i, read_back)
             comp.wait_stream(copy)
             comp.wait_stream(back)
             z.record(comp)
@@ -957,7 +957,7 @@ def measure_e2e(step, w: W.Workload, args, total_bytes: int, world: int):
             if n > 0:
                 readback.append((step.out_k[r, :n], host[0][r, :n]))
                 readback.append((step.out_v[r, :n], host[1][r, :n]))
-    wins_rb = windows(readback=True)
+    wins_rb = windows(read_back=True)
     ms_rb = max_over_ranks(float(np.median(wins_rb)), dev)
     d2h_rb = sum(src.numel() * src.element_size() for src, _ in readback) + 12
     step.k, step.v = bufs[0]
