@@ -909,12 +909,12 @@ def measure_e2e(step, w: W.Workload, args, total_bytes: int, world: int):
         torch.cuda.synchronize(dev)
         a = torch.cuda.Event(enable_timing=True)
         z = torch.cuda.Event(enable_timing=True)
-        # three timed windows of n steps; the median window is reported (the host link is
-        # shared with the rest of the machine, and one window can land on a burst of other
-        # traffic)
+        # five timed windows of n steps; the median window is reported (the host link is
+        # shared with the rest of the machine: a window that lands on a burst of other
+        # traffic runs up to 1.5x longer, while the quiet ones sit at the link's 211 GB/s)
         n = max(4, min(args.steps, 6))
         out = []
-        for _ in range(3):
+        for _ in range(5):
             a.record(comp)
             copy.wait_stream(comp)  # the timed copies start after the start event
             for i in range(n):
