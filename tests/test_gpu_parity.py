@@ -278,7 +278,7 @@ def test_device_bounds_flags():
 
 
 @pytest.mark.parametrize("numel", [0, 1, 15, 16, 17, 1000, 4096 * 7 + 5, 1 << 16, (1 << 16) + 1,
-                                   (1 << 16) + 31, 3 << 20])
+                                   (1 << 16) + 31, 3 << 20, 1 << 23, (1 << 23) + 3 * 8192 + 17])
 @pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
 def test_global_scale(numel, dt):
     import nvfp4_paged_kv_02_gb300 as nv
@@ -290,7 +290,7 @@ def test_global_scale(numel, dt):
         assert np.float32(got).view(np.uint32) == np.float32(want).view(np.uint32), (got, want)
 
 
-@pytest.mark.parametrize("numel", [1000, 1 << 16, (1 << 16) + 17, 1 << 20])
+@pytest.mark.parametrize("numel", [1000, 1 << 16, (1 << 16) + 17, 1 << 20, (1 << 23) + 5])
 @pytest.mark.parametrize("where", [0, -1, "mid"])
 def test_global_scale_max_at_edges(numel, where):
     """The tensor's largest magnitude (negative) at the first, last or a middle element, for
