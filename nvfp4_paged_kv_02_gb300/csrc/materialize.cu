@@ -239,7 +239,11 @@ __global__ void __launch_bounds__(kTmaThreads, 3) materialize_tma_kernel(const M
     int s = 0;
     uint32_t round = 0;  // how many times stage s has been used before
     ItemCursor cur;
-    if (lane == 0) cur.init(q, items_per_fetch(items, half_page));
+    if (lane == 0) {
+      // the last two batches' worth of items per CTA are taken one at a time
+      const int per = items_per_fetch(items, half_page);
+      cur.init(q, per, items - 2ll * per * gridDim.x);
+    }
     for (;; s = (s + 1 == ns) ? 0 : s + 1, round += (s == 0)) {
       // the next item, its source page and output page, resolved while the consumers still
       // work on the stage it will use

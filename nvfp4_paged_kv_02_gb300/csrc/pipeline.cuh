@@ -107,30 +107,38 @@ __host__ __device__ inline WorkQueue work_queue(void* workspace) {
 // million atomics a second, which small items would otherwise reach, and consecutive items
 // of one CTA write neighbouring output); in fixed shares one at a time. The next batch is
 // requested when the current one is started, so the atomic's latency overlaps the work on
-// the current items.
+// the current items. Batches requested from item `tail` on are single items, so that the
+// last wave ends more evenly.
 struct ItemCursor {
-  long long mine, base, next_base;
-  int i, per;
+  long long mine, base, next_base, tail;
+  int i, per, n, next_n;
 
-  __device__ __forceinline__ long long take(const WorkQueue& q) {
-    if (q.next) return static_cast<long long>(atomicAdd(q.next, static_cast<unsigned long long>(per)));
+  __device__ __forceinline__ long long take(const WorkQueue& q, int count) {
+    if (q.next) return static_cast<long long>(atomicAdd(q.next, static_cast<unsigned long long>(count)));
     const long long it = mine;
     mine += gridDim.x;
     return it;
   }
-  __device__ __forceinline__ void init(const WorkQueue& q, int items_per_fetch) {
+  __device__ __forceinline__ void init(const WorkQueue& q, int items_per_fetch,
+                                       long long tail_from = 0x7FFFFFFFFFFFFFFFll) {
     mine = blockIdx.x;
     i = 0;
     per = q.next ? (items_per_fetch > 0 ? items_per_fetch : 1) : 1;
+    tail = tail_from;
+    n = next_n = per;
     next_base = 0;
-    base = take(q);
+    base = take(q, n);
   }
   // The next item; one at or past `limit` means there is no more work.
   __device__ __forceinline__ long long next(const WorkQueue& q, long long limit) {
     const long long item = base + i;
-    if (i == 0 && item < limit) next_base = take(q);
-    if (++i == per) {
+    if (i == 0 && item < limit) {
+      next_n = item >= tail ? 1 : per;
+      next_base = take(q, next_n);
+    }
+    if (++i == n) {
       base = next_base;
+      n = next_n;
       i = 0;
     }
     return item;
