@@ -407,7 +407,11 @@ def active_pages(w: W.Workload) -> int:
 # the other configurations, measured after the headline step
 # ---------------------------------------------------------------------------------------
 
-SECONDARY = ("decode", "prefill", "materialize", "contig")
+# (key, workload, V-scale layout of the materialize input)
+SECONDARY = (("decode", "decode", "linear"), ("prefill", "prefill", "linear"),
+             ("materialize", "materialize", "linear"),
+             ("materialize_v_interleaved4", "materialize", "interleaved4"),
+             ("contig", "contig", "linear"))
 
 
 def time_ops(step, dev: torch.device, n_steps: int, warmup: int = 3):
@@ -524,13 +528,14 @@ def materialize_host_cost(step, n_calls: int = 200, layers: int = 32):
 
 
 def measure_configs(w_large: W.Workload, dev: torch.device, n_steps: int = 20):
-    """Per-op figures of the decode, prefill and materialize workloads and of the contiguous
-    form (on the large pool's K and V rows), each timed on its own after the headline step."""
+    """Per-op figures of the decode, prefill and materialize workloads (the last also with V
+    scales in the 4-token-interleaved layout) and of the contiguous form (on the large pool's
+    K and V rows), each timed on its own after the headline step."""
     peak, _ = measured_peaks()
     out = {}
-    for name in SECONDARY:
-        w = w_large if name == "contig" else make_workload(name, dev)
-        step = ContigStep(w, dev) if name == "contig" else Step(w, dev)
+    for name, wl, v_scales in SECONDARY:
+        w = w_large if wl == "contig" else make_workload(wl, dev)
+        step = ContigStep(w, dev) if wl == "contig" else Step(w, dev, v_scales)
         op_ms, small = time_ops(step, dev, n_steps)
         status = int(step.status.item())
         host = materialize_host_cost(step) if name == "materialize" else None
