@@ -12,6 +12,10 @@ Operations (FlashInfer documentation pages):
   NVFP4KVMaterializer          "flashinfer.quantization" index, NVFP4KVMaterializer
   nvfp4_make_global_scale      "flashinfer.quantization" index, make_nvfp4_global_scale
   nvfp4_e4m3_max               "flashinfer.quantization" index, nvfp4_e4m3_max
+  nvfp4_kv_quantize,           "flashinfer.quantization" index, FP4 KV Cache Quantization
+  nvfp4_kv_dequantize            (contiguous tensors, linear block scales)
+  nvfp4_4over6_code,           "flashinfer.quantization" index, NVFP4 4over6 Recipes
+  nvfp4_4over6_from_code         (the recipe as one int64)
 """
 
 from __future__ import annotations
