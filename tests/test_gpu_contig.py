@@ -158,3 +158,30 @@ def test_kv_quantize_large_sampled():
     assert np.array_equal(fp4[idx].cpu().numpy(), c)
     assert np.array_equal(sf[idx].cpu().numpy(), s)
     assert np.array_equal(W.bits16(y[idx].cpu()), O.kv_dequantize(c, s, gs, True))
+
+
+def test_kv_ops_past_2_gib_of_codes():
+    """4.3 M rows of 1024 elements: the codes (2.2 GB) and the output run past 2^31 bytes, so
+    every offset in both bulk-copy rings must be 64-bit. Sampled rows, the last ones
+    included, are compared with the oracle."""
+    import nvfp4_paged_kv_02_gb300 as nv
+    dev = torch.device("cuda")
+    rows, cols = 4_300_000, 1024
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(29)
+    x = torch.empty((rows, cols), dtype=torch.bfloat16, device=dev)
+    for r0 in range(0, rows, 1 << 20):  # in slices, to bound the binary32 temporaries
+        x[r0:r0 + (1 << 20)] = torch.randn((min(1 << 20, rows - r0), cols), generator=gen,
+                                           device=dev).mul_(2.0)
+    gs = float(np.float32(float(x.abs().max()) / 2688.0))
+    g = torch.tensor([gs], dtype=torch.float32, device=dev)
+    fp4, sf = nv.nvfp4_kv_quantize(x, g, None)
+    y = nv.nvfp4_kv_dequantize(fp4, sf, g, torch.bfloat16)
+    assert fp4.numel() > (1 << 31)
+    idx = torch.tensor(sorted(set(np.random.default_rng(31).integers(0, rows, 100).tolist())
+                              | {0, rows // 2, rows - 2, rows - 1}), device=dev)
+    xs = x[idx].cpu()
+    c, s = O.kv_quantize(W.bits16(xs), True, gs, None)
+    assert np.array_equal(fp4[idx].cpu().numpy(), c)
+    assert np.array_equal(sf[idx].cpu().numpy(), s)
+    assert np.array_equal(W.bits16(y[idx].cpu()), O.kv_dequantize(c, s, gs, True))
